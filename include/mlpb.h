@@ -1,0 +1,176 @@
+/*
+ * mlpb.h -- C ABI of libmlpb: the tensor-parallel transformer MLP block and
+ * the sequence-parallel LayerNorm on one GB300 (sm_103a).
+ *
+ * What the library computes.  "Megatron-LM" source tour (pyshine.com/megatron-lm),
+ * section "The Tensor-Parallel Primitives": fc1 is a ColumnParallelLinear (its
+ * weight split along the output dimension; every rank sees the full input),
+ * fc2 a RowParallelLinear (weight split along the input dimension, partial
+ * sums all-reduced at the end), so the block needs one all-reduce.  Section
+ * "The Transformer Stack": a fused bias-GELU sits between them; gated
+ * variants (SwiGLU) multiply a gate by an up projection.  "Megatron-LM /
+ * Megatron-Core" concept note, section "Key math / How it works": the
+ * conjugate operators f (identity forward, all-reduce backward) and g
+ * (all-reduce forward, identity backward), and sequence parallelism (LN split
+ * along the sequence, gathers and reduce-scatters at the GEMM boundaries).
+ *
+ * The t tensor-parallel ranks are emulated on one device as partitions of the
+ * weights.  The g all-reduce is the accumulation of all t shards' K-blocks
+ * into one tensor-memory accumulator in the fc2 GEMM; the f all-reduce of the
+ * backward is the same accumulation in the dX GEMM.  Sequence shards are
+ * contiguous row blocks, so the SP gather / reduce-scatter are index ranges.
+ *
+ *   GELU:   Z = X W1^T + b1, A = gelu_tanh(Z), Y = A W2^T + b2
+ *   SwiGLU: G = X Wg^T, U = X Wu^T, A = silu(G) * U, Y = A W2^T   (no biases)
+ *
+ * Conventions for every entry point
+ *   - Pointers named as tensors are DEVICE pointers, 16-byte aligned, owned by
+ *     the caller; the library never frees or retains them past the call.
+ *   - bf16 means IEEE bfloat16 (2 bytes); all matrices are row-major.
+ *   - Layouts (shard-major, as each tensor-parallel rank stores its slice):
+ *       X, Xn, dY           [T][H] bf16
+ *       W1 (GELU)           [t][Fs][H] bf16        W1 (SwiGLU) [t][2][Fs][H] (gate, up)
+ *       b1                  [F] bf16 (shard i owns b1[i*Fs .. (i+1)*Fs))
+ *       W2                  [t][H][Fs] bf16        b2 [H] bf16
+ *       Z saved (GELU)      [T][F]  bf16, column i*Fs+j = shard i, feature j
+ *       Z saved (SwiGLU)    [T][t][2][Fs] bf16 (G then U of each shard)
+ *       A saved             [T][F]  bf16
+ *       Y, dX               [T][H] fp32
+ *       dW1, dW2            fp32 in the layouts of W1, W2;  db1 [F], db2 [H] fp32
+ *     where T = tokens, H = hidden, F = ffn, t = tp, Fs = F / t.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Argument errors are returned synchronously and launch
+ *     nothing.  Outputs are overwritten, never accumulated into.
+ *   - A device-side bounded wait that expires (about one second) is recorded in
+ *     a per-handle error word and reported by mlpb_last_device_error().
+ *   - A handle may be used from one host thread at a time.
+ */
+#ifndef MLPB_H_
+#define MLPB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mlpb_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MLPB_OK = 0,
+  MLPB_EINVAL = -1,       /* null / misaligned pointer, bad config value          */
+  MLPB_EUNSUPPORTED = -2, /* shape outside the supported set (see mlpb_create)    */
+  MLPB_ECUDA = -3,        /* a CUDA runtime call or launch failed                 */
+  MLPB_ETIMEOUT = -4,     /* a device-side bounded wait expired (kernel bailed)   */
+  MLPB_ENOMEM = -5        /* host allocation failed                               */
+} mlpb_status;
+
+typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
+
+/* mlpb_config.flags */
+#define MLPB_FLAG_FAULT_INJECT 0x1u    /* test only: the first GEMM launch of the  \
+                                          next forward skips one producer arrive, so \
+                                          its consumers' bounded wait expires        */
+#define MLPB_FLAG_EMULATE_COPIES 0x2u  /* SP gather / reduce-scatter run as explicit \
+                                          in-device copy kernels (costs bandwidth)   */
+
+typedef struct {
+  int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */
+  int64_t hidden;          /* H: multiple of 64, >= 64                            */
+  int64_t ffn;             /* F: divisible by tp, with F/tp a multiple of 8       */
+  int32_t tp;              /* t: emulated tensor-parallel degree, 1..1024         */
+  int32_t act;             /* mlpb_act                                            */
+  int32_t has_bias;        /* GELU only: b1, b2 present (SwiGLU requires 0)       */
+  int32_t seq_parallel_ln; /* LN entry points enabled; requires T % t == 0        */
+  float ln_eps;            /* LayerNorm epsilon (inside the square root)          */
+  uint32_t flags;          /* MLPB_FLAG_*                                         */
+} mlpb_config;
+
+typedef struct mlpb_handle mlpb_handle; /* opaque; owns no tensors */
+
+/* Per-kernel timing record (filled when timing is enabled). */
+typedef struct {
+  char name[32];  /* kernel name, e.g. "fc1_gelu", "colsum_db2"                  */
+  float ms;       /* device time between CUDA events recorded around the launch   */
+  double flops;   /* algorithmic GEMM flops of the launch (0 for memory kernels)  */
+  double bytes;   /* algorithmic HBM bytes of the launch (minimum reads + writes) */
+} mlpb_kernel_time;
+
+/* Validates *cfg, queries the current device and allocates the 4-byte device
+ * error word.  Returns EINVAL for a null argument or an out-of-range field,
+ * EUNSUPPORTED for shapes outside: T % 128 == 0, H % 64 == 0 and H >= 64,
+ * F % tp == 0 and (F/tp) % 8 == 0, SwiGLU without bias, SP with T % tp == 0
+ * and H <= 16384.  On success *out owns host state only. */
+mlpb_status mlpb_create(const mlpb_config *cfg, mlpb_handle **out);
+
+/* Frees the handle and its error word.  NULL is ignored. */
+void mlpb_destroy(mlpb_handle *h);
+
+/* Bytes of device scratch the caller passes as `workspace` to mlpb_backward and
+ * mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16 and reduction partials). */
+mlpb_status mlpb_workspace_size(const mlpb_handle *h, size_t *bytes);
+
+/* Bytes of the saved activations: z_bytes for Z (GELU, T*F*2) or G|U (SwiGLU,
+ * T*2F*2); a_bytes for A (T*F*2). */
+mlpb_status mlpb_saved_size(const mlpb_handle *h, size_t *z_bytes, size_t *a_bytes);
+
+/* Forward of the block ("The Tensor-Parallel Primitives" and "The Transformer
+ * Stack" of the source tour; f and g of "Key math").  fc1 over all t column
+ * shards with the fused bias+GELU or SwiGLU epilogue writes Zsaved and Asaved;
+ * fc2 accumulates all t row shards into one accumulator per output tile (the
+ * emulated g all-reduce) and adds b2 once, writing Y [T][H] fp32.  b1 and b2
+ * must be NULL when has_bias is 0. */
+mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const void *b1,
+                         const void *W2, const void *b2, float *Y, void *Zsaved,
+                         void *Asaved, void *workspace, mlpb_stream_t stream);
+
+/* Backward of the block for an upstream gradient dY [T][H] bf16.  g backward is
+ * the identity (every shard reads the same dY); dZ = (dY W2_i) * act'(.) per
+ * shard; dW2_i = dY^T A_i; dW1_i = dZ_i^T X; db1 = sum_t dZ; db2 = sum_t dY;
+ * dX = sum_i dZ_i W1_i with the sum over shards accumulated in one tensor-memory
+ * accumulator (the emulated f all-reduce).  db1/db2 must be NULL without bias.
+ * `workspace` must hold mlpb_workspace_size() bytes. */
+mlpb_status mlpb_backward(mlpb_handle *h, const void *X, const void *W1, const void *W2,
+                          const void *Zsaved, const void *Asaved, const void *dY,
+                          float *dX, float *dW1, float *dW2, float *db1, float *db2,
+                          void *workspace, mlpb_stream_t stream);
+
+/* Sequence-parallel LayerNorm forward ("The Tensor-Parallel Primitives": norms
+ * run on sequence-sharded activations).  Shard s owns rows [s*T/t, (s+1)*T/t);
+ * each row r gets mean[r], rstd[r] = 1/sqrt(var + eps) (biased variance) and
+ * Xn[r] = (X[r]-mean)*rstd*gamma + beta in bf16.  The emulated all-gather is
+ * the row-block layout of Xn itself (or a copy kernel with EMULATE_COPIES).
+ * X, gamma, beta bf16; mean, rstd [T] fp32.  Requires seq_parallel_ln. */
+mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle *h, const void *X, const void *gamma,
+                                  const void *beta, void *Xn, float *mean, float *rstd,
+                                  mlpb_stream_t stream);
+
+/* Sequence-parallel LayerNorm backward for dXn [T][H] fp32 (the dX output of
+ * mlpb_backward run on Xn).  dX [T][H] fp32; dgamma, dbeta [H] fp32 are the sum
+ * over shards of each shard's partials (the all-reduce the SP layout implies).
+ * `workspace` must hold mlpb_workspace_size() bytes. */
+mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle *h, const void *X, const void *gamma,
+                                  const float *mean, const float *rstd, const float *dXn,
+                                  float *dX, float *dgamma, float *dbeta, void *workspace,
+                                  mlpb_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the device error word.  Returns
+ * MLPB_ETIMEOUT if a bounded wait expired since the last call, MLPB_ECUDA if
+ * the stream reported an error, else MLPB_OK. */
+mlpb_status mlpb_last_device_error(mlpb_handle *h, mlpb_stream_t stream);
+
+/* Enables (1) or disables (0) per-kernel CUDA-event timing on the handle. */
+mlpb_status mlpb_enable_timing(mlpb_handle *h, int enable);
+
+/* Copies up to `capacity` timing records of the launches since the last read
+ * (waiting on their events), sets *count, and clears the list. */
+mlpb_status mlpb_read_timings(mlpb_handle *h, mlpb_kernel_time *out, int capacity, int *count);
+
+/* Static English text of a status code. */
+const char *mlpb_status_str(mlpb_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLPB_H_ */

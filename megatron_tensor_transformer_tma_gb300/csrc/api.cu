@@ -1,0 +1,578 @@
+// C ABI of libmlpb: handle, validation, tensor-map encoding, launch plans, timing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/mlpb.h"
+#include "kernels.h"
+
+using namespace mlpb;
+
+namespace {
+
+struct TimedLaunch {
+  char name[32];
+  double flops, bytes;
+  cudaEvent_t start, stop;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+mlpb_status load_encoder() {
+  std::lock_guard<std::mutex> lock(g_encode_mu);
+  if (g_encode != nullptr) return MLPB_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return MLPB_ECUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return MLPB_OK;
+}
+
+// A bf16 tensor map with 128-byte swizzle.  dims[0] is the contiguous dimension;
+// strides_bytes[k] is the byte stride of dimension k+1.
+bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int k = 0; k < rank; ++k) {
+    gd[k] = dims[k];
+    bx[k] = box[k];
+    es[k] = 1;
+    if (k + 1 < rank) gs[k] = strides_bytes[k];
+  }
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool map2d(CUtensorMap* m, const void* p, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+           uint32_t box_inner, uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t str[1] = {ld_elems * 2};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_bf16(m, p, 2, dims, str, box);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+struct mlpb_handle {
+  mlpb_config cfg;
+  int64_t T, H, F, Fs, F1;
+  int t;
+  bool swiglu;
+  int device;
+  int num_sms;
+  uint32_t* d_err;
+  bool fault_pending;
+  uint64_t wait_ns;
+  // bias-grad split plans
+  int db2_splits, db1_splits;
+  int64_t db2_rows, db1_rows;
+  int ln_blocks_per_shard;
+  // timing
+  bool timing;
+  std::vector<TimedLaunch> launches;
+  std::vector<cudaEvent_t> event_pool;
+
+  cudaEvent_t take_event() {
+    if (!event_pool.empty()) {
+      cudaEvent_t e = event_pool.back();
+      event_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+
+namespace {
+
+// Brackets one launch with CUDA events on its stream when timing is enabled.
+struct LaunchTimer {
+  mlpb_handle* h;
+  cudaStream_t s;
+  TimedLaunch rec{};
+  LaunchTimer(mlpb_handle* h_, cudaStream_t s_, const char* name, double flops, double bytes)
+      : h(h_), s(s_) {
+    if (!h->timing) return;
+    std::snprintf(rec.name, sizeof(rec.name), "%s", name);
+    rec.flops = flops;
+    rec.bytes = bytes;
+    rec.start = h->take_event();
+    rec.stop = h->take_event();
+    cudaEventRecord(rec.start, s);
+  }
+  void done() {
+    if (!h->timing) return;
+    cudaEventRecord(rec.stop, s);
+    h->launches.push_back(rec);
+  }
+};
+
+mlpb_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLPB_OK : MLPB_ECUDA; }
+
+GemmParams base_params(const mlpb_handle* h) {
+  GemmParams p{};
+  p.T = static_cast<int>(h->T);
+  p.H = static_cast<int>(h->H);
+  p.F = static_cast<int>(h->F);
+  p.Fs = static_cast<int>(h->Fs);
+  p.t = h->t;
+  p.err = h->d_err;
+  p.wait_ns = h->wait_ns;
+  p.kb_per_shard = static_cast<int>(cdiv(h->Fs, kBK));
+  return p;
+}
+
+mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap& a,
+                     const CUtensorMap& b, const GemmParams& p, cudaStream_t s, const char* name,
+                     double flops, double bytes) {
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  if (tiles == 0) return MLPB_OK;
+  const int grid = std::min(tiles, h->num_sms);
+  LaunchTimer lt(h, s, name, flops, bytes);
+  cudaError_t e = fwd ? launch_gemm_fwd(kind, a, b, p, grid, s) : launch_gemm_bwd(kind, a, b, p, grid, s);
+  lt.done();
+  return from_cuda(e);
+}
+
+size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
+
+size_t ws_backward_bytes(const mlpb_handle* h) {
+  size_t b = ws_dz_bytes(h);
+  if (h->cfg.has_bias) {
+    b += align256(static_cast<size_t>(h->db2_splits) * h->H * 4);
+    b += align256(static_cast<size_t>(h->db1_splits) * h->F * 4);
+  }
+  return b;
+}
+
+size_t ws_ln_bytes(const mlpb_handle* h) {
+  if (!h->cfg.seq_parallel_ln) return 0;
+  const size_t nblk = static_cast<size_t>(h->t) * h->ln_blocks_per_shard;
+  return 2 * align256(nblk * h->H * 4);
+}
+
+void plan_colsum(int64_t R, int64_t C, int num_sms, int* splits, int64_t* rows) {
+  const int64_t chunks = std::max<int64_t>(1, cdiv(C, 512));
+  int64_t s = cdiv(4 * num_sms, chunks);
+  s = std::max<int64_t>(1, std::min<int64_t>(s, std::max<int64_t>(1, R / 16)));
+  int64_t rp = std::max<int64_t>(1, cdiv(R, s));
+  *rows = rp;
+  *splits = static_cast<int>(std::max<int64_t>(1, cdiv(R, rp)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mlpb_status_str(mlpb_status s) {
+  switch (s) {
+    case MLPB_OK: return "ok";
+    case MLPB_EINVAL: return "invalid argument";
+    case MLPB_EUNSUPPORTED: return "unsupported shape or configuration";
+    case MLPB_ECUDA: return "CUDA error";
+    case MLPB_ETIMEOUT: return "device-side bounded wait expired";
+    case MLPB_ENOMEM: return "out of host memory";
+  }
+  return "unknown status";
+}
+
+mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
+  if (cfg == nullptr || out == nullptr) return MLPB_EINVAL;
+  *out = nullptr;
+  const mlpb_config& c = *cfg;
+  if (c.tokens < 0 || c.hidden <= 0 || c.ffn <= 0 || c.tp < 1 || c.tp > 1024) return MLPB_EINVAL;
+  if (c.act != MLPB_ACT_GELU_TANH && c.act != MLPB_ACT_SWIGLU) return MLPB_EINVAL;
+  if (c.has_bias != 0 && c.has_bias != 1) return MLPB_EINVAL;
+  if (c.seq_parallel_ln != 0 && c.seq_parallel_ln != 1) return MLPB_EINVAL;
+  if ((c.flags & ~MLPB_FLAG_FAULT_INJECT) != 0) return MLPB_EINVAL;
+  if (c.seq_parallel_ln && !(c.ln_eps > 0.f)) return MLPB_EINVAL;
+  if (c.tokens % 128 != 0 || c.hidden % 64 != 0) return MLPB_EUNSUPPORTED;
+  if (c.ffn % c.tp != 0 || (c.ffn / c.tp) % 8 != 0) return MLPB_EUNSUPPORTED;
+  if (c.act == MLPB_ACT_SWIGLU && c.has_bias) return MLPB_EUNSUPPORTED;
+  if (c.seq_parallel_ln && (c.tokens % c.tp != 0 || c.hidden > 16384)) return MLPB_EUNSUPPORTED;
+  const int64_t f1 = c.act == MLPB_ACT_SWIGLU ? 2 * c.ffn : c.ffn;
+  // int32 tile/coordinate arithmetic inside the kernels
+  if (c.tokens > (int64_t(1) << 30) || c.hidden > (int64_t(1) << 30) || f1 > (int64_t(1) << 30))
+    return MLPB_EUNSUPPORTED;
+
+  mlpb_handle* h = new (std::nothrow) mlpb_handle();
+  if (h == nullptr) return MLPB_ENOMEM;
+  h->cfg = c;
+  h->T = c.tokens;
+  h->H = c.hidden;
+  h->F = c.ffn;
+  h->t = c.tp;
+  h->Fs = c.ffn / c.tp;
+  h->swiglu = c.act == MLPB_ACT_SWIGLU;
+  h->F1 = f1;
+  h->fault_pending = (c.flags & MLPB_FLAG_FAULT_INJECT) != 0;
+  h->wait_ns = 1000000000ull;
+  h->timing = false;
+  h->d_err = nullptr;
+
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+          cudaSuccess) {
+    delete h;
+    return MLPB_ECUDA;
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  if (major != 10 || minor != 3) {  // the kernels are built for sm_103a only
+    delete h;
+    return MLPB_EUNSUPPORTED;
+  }
+  if (load_encoder() != MLPB_OK || gemm_fwd_set_smem_attrs() != cudaSuccess ||
+      gemm_bwd_set_smem_attrs() != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return MLPB_ECUDA;
+  }
+  plan_colsum(h->T, h->H, h->num_sms, &h->db2_splits, &h->db2_rows);
+  plan_colsum(h->T, h->F, h->num_sms, &h->db1_splits, &h->db1_rows);
+  h->ln_blocks_per_shard =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(h->num_sms, h->t),
+                                                               h->t ? h->T / h->t : 1)));
+  *out = h;
+  return MLPB_OK;
+}
+
+void mlpb_destroy(mlpb_handle* h) {
+  if (h == nullptr) return;
+  for (auto& l : h->launches) {
+    cudaEventDestroy(l.start);
+    cudaEventDestroy(l.stop);
+  }
+  for (auto e : h->event_pool) cudaEventDestroy(e);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+}
+
+mlpb_status mlpb_workspace_size(const mlpb_handle* h, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr) return MLPB_EINVAL;
+  *bytes = std::max<size_t>(std::max(ws_backward_bytes(h), ws_ln_bytes(h)), 256);
+  return MLPB_OK;
+}
+
+mlpb_status mlpb_saved_size(const mlpb_handle* h, size_t* z_bytes, size_t* a_bytes) {
+  if (h == nullptr || z_bytes == nullptr || a_bytes == nullptr) return MLPB_EINVAL;
+  *z_bytes = static_cast<size_t>(h->T * h->F1 * 2);
+  *a_bytes = static_cast<size_t>(h->T * h->F * 2);
+  return MLPB_OK;
+}
+
+mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                         const void* W2, const void* b2, float* Y, void* Zsaved, void* Asaved,
+                         void* workspace, mlpb_stream_t stream) {
+  (void)workspace;
+  if (h == nullptr) return MLPB_EINVAL;
+  const bool bias = h->cfg.has_bias != 0;
+  if (!X || !W1 || !W2 || !Y || !Zsaved || !Asaved) return MLPB_EINVAL;
+  if (bias != (b1 != nullptr) || bias != (b2 != nullptr)) return MLPB_EINVAL;
+  for (const void* p : {X, W1, W2, static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
+                        static_cast<const void*>(Asaved), b1, b2})
+    if (p && !aligned16(p)) return MLPB_EINVAL;
+  if (h->T == 0) return MLPB_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t;
+
+  // ---- fc1 (column-parallel; f forward = every shard reads the same X)
+  CUtensorMap ta, tb;
+  GemmParams p = base_params(h);
+  p.M = static_cast<int>(T);
+  p.num_m_tiles = static_cast<int>(T / kBM);
+  p.num_kb = static_cast<int>(cdiv(H, kBK));
+  p.out0 = Zsaved;
+  p.out1 = Asaved;
+  p.fault_inject = h->fault_pending ? 1 : 0;
+  h->fault_pending = false;
+  if (!map2d(&ta, X, H, T, H, kBK, kBM)) return MLPB_EINVAL;
+  mlpb_status st;
+  if (!h->swiglu) {
+    if (!map2d(&tb, W1, H, F, H, kBK, kBN)) return MLPB_EINVAL;
+    p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
+    p.bias = static_cast<const __nv_bfloat16*>(b1);
+    st = run_gemm(h, GemmKind::FC1_GELU, true, ta, tb, p, s, "fc1_gelu", 2.0 * T * F * H,
+                  2.0 * (T * H + F * H + 2 * T * F) + (bias ? 2.0 * F : 0.0));
+  } else {
+    const uint64_t dims[4] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs), 2,
+                              static_cast<uint64_t>(t)};
+    const uint64_t str[3] = {static_cast<uint64_t>(H * 2), static_cast<uint64_t>(Fs * H * 2),
+                             static_cast<uint64_t>(2 * Fs * H * 2)};
+    const uint32_t box[4] = {kBK, 128, 1, 1};
+    if (!encode_bf16(&tb, W1, 4, dims, str, box)) return MLPB_EINVAL;
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    st = run_gemm(h, GemmKind::FC1_SWIGLU, true, ta, tb, p, s, "fc1_swiglu", 4.0 * T * F * H,
+                  2.0 * (T * H + 2 * F * H + 3 * T * F));
+  }
+  if (st != MLPB_OK) return st;
+
+  // ---- fc2 (row-parallel; g forward = all t shards accumulate into one TMEM tile)
+  {
+    const uint64_t adims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
+                               static_cast<uint64_t>(t)};
+    const uint64_t astr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
+    const uint32_t abox[3] = {kBK, kBM, 1};
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
+                               static_cast<uint64_t>(t)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
+    const uint32_t bbox[3] = {kBK, kBN, 1};
+    if (!encode_bf16(&ta, Asaved, 3, adims, astr, abox) ||
+        !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
+      return MLPB_EINVAL;
+    GemmParams q = base_params(h);
+    q.M = static_cast<int>(T);
+    q.num_m_tiles = static_cast<int>(T / kBM);
+    q.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    q.num_kb = static_cast<int>(t * q.kb_per_shard);
+    q.bias = static_cast<const __nv_bfloat16*>(b2);
+    q.out0 = Y;
+    st = run_gemm(h, GemmKind::FC2, true, ta, tb, q, s, "fc2", 2.0 * T * H * F,
+                  2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0));
+  }
+  return st;
+}
+
+mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const void* W2,
+                          const void* Zsaved, const void* Asaved, const void* dY, float* dX,
+                          float* dW1, float* dW2, float* db1, float* db2, void* workspace,
+                          mlpb_stream_t stream) {
+  if (h == nullptr) return MLPB_EINVAL;
+  const bool bias = h->cfg.has_bias != 0;
+  if (!X || !W1 || !W2 || !Zsaved || !Asaved || !dY || !dX || !dW1 || !dW2 || !workspace)
+    return MLPB_EINVAL;
+  if (bias != (db1 != nullptr) || bias != (db2 != nullptr)) return MLPB_EINVAL;
+  for (const void* p : {X, W1, W2, Zsaved, Asaved, dY, static_cast<const void*>(dX),
+                        static_cast<const void*>(dW1), static_cast<const void*>(dW2),
+                        static_cast<const void*>(db1), static_cast<const void*>(db2),
+                        static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return MLPB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
+  mlpb_status st = MLPB_OK;
+
+  if (T == 0) {  // empty batch: every parameter gradient is zero
+    st = from_cuda(launch_fill_zero(dW1, static_cast<size_t>(F1 * H * 4), s));
+    if (st == MLPB_OK) st = from_cuda(launch_fill_zero(dW2, static_cast<size_t>(F * H * 4), s));
+    if (st == MLPB_OK && bias) st = from_cuda(launch_fill_zero(db1, static_cast<size_t>(F * 4), s));
+    if (st == MLPB_OK && bias) st = from_cuda(launch_fill_zero(db2, static_cast<size_t>(H * 4), s));
+    return st;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* dZ = ws;
+  float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
+  float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
+                                          align256(static_cast<size_t>(h->db2_splits) * H * 4));
+
+  // ---- db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
+  if (bias) {
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H);
+    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s);
+    lt.done();
+    if ((st = from_cuda(e)) != MLPB_OK) return st;
+  }
+
+  CUtensorMap ta, tb;
+  // ---- dgrad of fc2 with the fused activation derivative: dZ [T][F1]
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(T);
+    p.num_m_tiles = static_cast<int>(T / kBM);
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_kb = static_cast<int>(cdiv(H, kBK));
+    p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
+    p.out0 = dZ;
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
+                               static_cast<uint64_t>(t)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
+    const uint32_t bbox[3] = {64, kBK, 1};
+    if (!map2d(&ta, dY, H, T, H, kBK, kBM) || !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
+      return MLPB_EINVAL;
+    const double bytes = 2.0 * (T * H + F * H + 2 * T * F1);
+    st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, ta, tb, p,
+                  s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H, bytes);
+    if (st != MLPB_OK) return st;
+  }
+
+  // ---- db1 = sum_t dZ
+  if (bias) {
+    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F);
+    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s);
+    lt.done();
+    if ((st = from_cuda(e)) != MLPB_OK) return st;
+  }
+
+  // ---- dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(H);
+    p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_kb = static_cast<int>(T / kBK);
+    p.out0 = dW2;
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
+                               static_cast<uint64_t>(t)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
+    const uint32_t bbox[3] = {64, kBK, 1};
+    if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
+      return MLPB_EINVAL;
+    st = run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s, "wgrad_w2", 2.0 * H * F * T,
+                  2.0 * (T * H + T * F) + 4.0 * H * F);
+    if (st != MLPB_OK) return st;
+  }
+
+  // ---- dW1 = dZ^T X  (M = F1, N = H, K = T)
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(F1);
+    p.num_m_tiles = static_cast<int>(cdiv(F1, kBM));
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    p.num_kb = static_cast<int>(T / kBK);
+    p.out0 = dW1;
+    if (!map2d(&ta, dZ, F1, T, F1, 64, kBK) || !map2d(&tb, X, H, T, H, 64, kBK))
+      return MLPB_EINVAL;
+    st = run_gemm(h, GemmKind::WGRAD_W1, false, ta, tb, p, s, "wgrad_w1", 2.0 * F1 * H * T,
+                  2.0 * (T * F1 + T * H) + 4.0 * F1 * H);
+    if (st != MLPB_OK) return st;
+  }
+
+  // ---- dX = sum_i dZ_i W1_i  (f backward: the sum over shards is the K loop)
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(T);
+    p.num_m_tiles = static_cast<int>(T / kBM);
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    p.num_kb = static_cast<int>(cdiv(F1, kBK));
+    p.out0 = dX;
+    if (!map2d(&ta, dZ, F1, T, F1, kBK, kBM) || !map2d(&tb, W1, H, F1, H, 64, kBK))
+      return MLPB_EINVAL;
+    st = run_gemm(h, GemmKind::DX, false, ta, tb, p, s, "dgrad_x", 2.0 * T * H * F1,
+                  2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+  }
+  return st;
+}
+
+mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle* h, const void* X, const void* gamma,
+                                  const void* beta, void* Xn, float* mean, float* rstd,
+                                  mlpb_stream_t stream) {
+  if (h == nullptr || !X || !gamma || !beta || !Xn || !mean || !rstd) return MLPB_EINVAL;
+  if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
+  for (const void* p : {X, gamma, beta, static_cast<const void*>(Xn)})
+    if (!aligned16(p)) return MLPB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = h->T, H = h->H;
+  LaunchTimer lt(h, s, "ln_fwd", 0.0, 4.0 * T * H + 8.0 * T + 4.0 * H);
+  cudaError_t e = launch_ln_fwd(X, gamma, beta, Xn, mean, rstd, T, H, h->cfg.ln_eps, s);
+  lt.done();
+  return from_cuda(e);
+}
+
+mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gamma,
+                                  const float* mean, const float* rstd, const float* dXn,
+                                  float* dX, float* dgamma, float* dbeta, void* workspace,
+                                  mlpb_stream_t stream) {
+  if (h == nullptr || !X || !gamma || !mean || !rstd || !dXn || !dX || !dgamma || !dbeta ||
+      !workspace)
+    return MLPB_EINVAL;
+  if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
+  for (const void* p : {X, gamma, static_cast<const void*>(dXn), static_cast<const void*>(dX),
+                        static_cast<const void*>(workspace)})
+    if (!aligned16(p)) return MLPB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = h->T, H = h->H;
+  const int nblk = h->t * h->ln_blocks_per_shard;
+  float* pg = static_cast<float*>(workspace);
+  float* pb = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       align256(static_cast<size_t>(nblk) * H * 4));
+  if (T == 0) {
+    cudaError_t e = launch_fill_zero(dgamma, static_cast<size_t>(H * 4), s);
+    if (e == cudaSuccess) e = launch_fill_zero(dbeta, static_cast<size_t>(H * 4), s);
+    return from_cuda(e);
+  }
+  LaunchTimer lt(h, s, "ln_bwd", 0.0, 10.0 * T * H + 8.0 * T + 10.0 * H);
+  cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dX, pg, pb, T, H, h->t,
+                                h->ln_blocks_per_shard, s);
+  lt.done();
+  if (e == cudaSuccess) {
+    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H);
+    e = launch_sum_partials(pg, nblk, H, dgamma, s);
+    if (e == cudaSuccess) e = launch_sum_partials(pb, nblk, H, dbeta, s);
+    lt2.done();
+  }
+  return from_cuda(e);
+}
+
+mlpb_status mlpb_last_device_error(mlpb_handle* h, mlpb_stream_t stream) {
+  if (h == nullptr) return MLPB_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLPB_ECUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, h->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLPB_ECUDA;
+  if (v != 0) {
+    if (cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) return MLPB_ECUDA;
+    return MLPB_ETIMEOUT;
+  }
+  return MLPB_OK;
+}
+
+mlpb_status mlpb_enable_timing(mlpb_handle* h, int enable) {
+  if (h == nullptr) return MLPB_EINVAL;
+  h->timing = enable != 0;
+  return MLPB_OK;
+}
+
+mlpb_status mlpb_read_timings(mlpb_handle* h, mlpb_kernel_time* out, int capacity, int* count) {
+  if (h == nullptr || count == nullptr || (capacity > 0 && out == nullptr)) return MLPB_EINVAL;
+  int n = 0;
+  mlpb_status st = MLPB_OK;
+  for (auto& l : h->launches) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(l.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, l.start, l.stop) != cudaSuccess)
+      st = MLPB_ECUDA;
+    if (n < capacity) {
+      std::memcpy(out[n].name, l.name, sizeof(out[n].name));
+      out[n].ms = ms;
+      out[n].flops = l.flops;
+      out[n].bytes = l.bytes;
+      ++n;
+    }
+    h->event_pool.push_back(l.start);
+    h->event_pool.push_back(l.stop);
+  }
+  h->launches.clear();
+  *count = n;
+  return st;
+}
+
+}  // extern "C"

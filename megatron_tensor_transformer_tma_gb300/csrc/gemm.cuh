@@ -1,0 +1,472 @@
+// Persistent, warp-specialised tcgen05 GEMM for the MLP block's six contractions.
+//
+// One CTA per SM (192 threads):
+//   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
+//               (128-byte swizzle) and arms the stage's mbarrier with the byte count;
+//   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
+//               N=256, K=16) from one thread into one of two 256-column fp32
+//               accumulators, committing each consumed stage back to the producer;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp owns the 32 TMEM lanes
+//               of its warp-id modulo 4), apply the fused pointwise op, store to HBM,
+//               then release the accumulator so the next tile's K loop can run.
+// Every wait is bounded (common.cuh): a wait that expires raises the CTA's abort flag
+// and the device error word; all roles then drain what they issued and free TMEM.
+//
+// The contractions (T tokens, H hidden, F ffn, t shards, Fs = F/t, F1 = F or 2F):
+//   FC1_GELU      Z = X W1^T + b1, A = gelu(Z)       M=T  N=F      K=H   A,B K-major
+//   FC1_SWIGLU    [G|U] = X [Wg_i|Wu_i]^T, A = silu(G)U  (per shard i, 128 gate + 128 up
+//                 columns per tile, one N=256 MMA)    M=T  N=2F     K=H
+//   FC2           Y = sum_i A_i W2_i^T + b2           M=T  N=H      K=t x Fs (walks shards)
+//   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B MN-major
+//   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B MN-major
+//   DX            dX = sum_i dZ_i W1_i                M=T  N=H      K=F1  B MN-major
+//   WGRAD_W2      dW2_i = dY^T A_i                    M=H  N=F      K=T   A,B MN-major
+//   WGRAD_W1      dW1 = dZ^T X                        M=F1 N=H      K=T   A,B MN-major
+#pragma once
+
+#include "common.cuh"
+#include "gemm_params.h"
+
+namespace mlpb {
+
+template <GemmKind K>
+struct KindOf {
+  static constexpr bool a_mn = (K == GemmKind::WGRAD_W2 || K == GemmKind::WGRAD_W1);
+  static constexpr bool b_mn = (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU ||
+                                K == GemmKind::DX || K == GemmKind::WGRAD_W2 ||
+                                K == GemmKind::WGRAD_W1);
+};
+
+// Grouped rasterisation: 8 consecutive M tiles sweep all N tiles together so that the
+// B tiles they share stay in L2.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& mt, int& nt) {
+  constexpr int G = 8;
+  const int span = G * p.num_n_tiles;
+  const int g = tile / span;
+  const int m0 = g * G;
+  const int gm = min(p.num_m_tiles - m0, G);
+  const int r = tile - g * span;
+  mt = m0 + r % gm;
+  nt = r / gm;
+}
+
+template <GemmKind K>
+__device__ __forceinline__ void issue_stage(const CUtensorMap* tA, const CUtensorMap* tB,
+                                            uint32_t sa, uint32_t sb, uint32_t bar, int mt,
+                                            int nt, int kb, const GemmParams& p) {
+  const int k0 = kb * kBK;
+  if constexpr (K == GemmKind::FC1_GELU) {
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_2d(sb, tB, bar, k0, nt * kBN);
+  } else if constexpr (K == GemmKind::FC1_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * 128;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_4d(sb, tB, bar, k0, j0, 0, i);            // gate rows -> B rows 0..127
+    tma_load_4d(sb + kBStage / 2, tB, bar, k0, j0, 1, i);  // up rows -> B rows 128..255
+  } else if constexpr (K == GemmKind::FC2) {
+    const int i = kb / p.kb_per_shard;
+    const int j0 = (kb - i * p.kb_per_shard) * kBK;
+    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
+    tma_load_3d(sb, tB, bar, j0, nt * kBN, i);
+  } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+  } else if constexpr (K == GemmKind::DX) {
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+  } else if constexpr (K == GemmKind::WGRAD_W2) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+  } else {  // WGRAD_W1
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+  }
+}
+
+// ------------------------------------------------------------------ pointwise math
+// tanh-form GELU written as z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), which is
+// the same function (1 + tanh(u) = 2 sigmoid(2u)) without cancellation for z << 0.
+constexpr float kSqrt2OverPi = 0.7978845608028654f;
+constexpr float kGeluCubic = 0.044715f;
+
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float gelu_f(float z) {
+  const float u = kSqrt2OverPi * (z + kGeluCubic * z * z * z);
+  return z * sigmoid_f(2.0f * u);
+}
+
+__device__ __forceinline__ float gelu_grad_f(float z) {
+  const float z2 = z * z;
+  const float u = kSqrt2OverPi * (z + kGeluCubic * z2 * z);
+  const float s = sigmoid_f(2.0f * u);
+  return s + 2.0f * z * s * (1.0f - s) * kSqrt2OverPi * (1.0f + 3.0f * kGeluCubic * z2);
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (q * 8 < nvalid) u = ld_global_nc_v4(p + q * 8);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      v[q * 8 + 2 * e] = f.x;
+      v[q * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < nvalid) {
+      uint4 u;
+      u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      st_global_v4(p + q * 8, u);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_f32x32(float* p, int nvalid, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (q * 4 < nvalid) {
+      uint4 u = make_uint4(__float_as_uint(v[q * 4 + 0]), __float_as_uint(v[q * 4 + 1]),
+                           __float_as_uint(v[q * 4 + 2]), __float_as_uint(v[q * 4 + 3]));
+      st_global_v4(p + q * 4, u);
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_load_f32x32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+// Epilogue of one 128 x 256 tile for the calling thread's row.  `tacc` is the TMEM
+// address of the accumulator at this warp's lane quarter.  All branches that skip
+// tcgen05.ld are uniform across the warp.
+template <GemmKind K>
+__device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, int nt,
+                                              const GemmParams& p) {
+  const int m = mt * kBM + row;
+  const bool row_ok = m < p.M;
+  if constexpr (K == GemmKind::FC1_GELU) {
+    const int n0 = nt * kBN;
+    __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * p.F;
+    __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= p.F) break;
+      float v[32];
+      tmem_load_f32x32(tacc + c * 32, v);
+      const int nv = min(32, p.F - col);
+      if (p.bias != nullptr) {
+        float b[32];
+        load_bf16x32(p.bias + col, nv, b);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += b[e];
+      }
+      if (row_ok) store_bf16x32(Z + col, nv, v);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
+      if (row_ok) store_bf16x32(A + col, nv, v);
+    }
+  } else if constexpr (K == GemmKind::FC1_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * 128;
+    __nv_bfloat16* GU = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * 2 * p.F +
+                        static_cast<size_t>(i) * 2 * p.Fs;
+    __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F +
+                       static_cast<size_t>(i) * p.Fs;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int jc = j0 + c * 32;
+      if (jc >= p.Fs) break;
+      float g[32], u[32];
+      tmem_load_f32x32(tacc + c * 32, g);
+      tmem_load_f32x32(tacc + 128 + c * 32, u);
+      const int nv = min(32, p.Fs - jc);
+      if (row_ok) {
+        store_bf16x32(GU + jc, nv, g);
+        store_bf16x32(GU + p.Fs + jc, nv, u);
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) u[e] *= g[e] * sigmoid_f(g[e]);
+      if (row_ok) store_bf16x32(A + jc, nv, u);
+    }
+  } else if constexpr (K == GemmKind::FC2 || K == GemmKind::DX) {
+    const int n0 = nt * kBN;
+    float* Y = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= p.H) break;
+      float v[32];
+      tmem_load_f32x32(tacc + c * 32, v);
+      const int nv = min(32, p.H - col);
+      if (K == GemmKind::FC2 && p.bias != nullptr) {
+        float b[32];
+        load_bf16x32(p.bias + col, nv, b);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += b[e];
+      }
+      if (row_ok) store_f32x32(Y + col, nv, v);
+    }
+  } else if constexpr (K == GemmKind::DGRAD_GELU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
+    const size_t base = static_cast<size_t>(m) * p.F + static_cast<size_t>(i) * p.Fs;
+    const __nv_bfloat16* Z = p.aux + base;
+    __nv_bfloat16* dZ = static_cast<__nv_bfloat16*>(p.out0) + base;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int jc = j0 + c * 32;
+      if (jc >= p.Fs) break;
+      float v[32], z[32];
+      tmem_load_f32x32(tacc + c * 32, v);
+      const int nv = min(32, p.Fs - jc);
+      if (row_ok) {
+        load_bf16x32(Z + jc, nv, z);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
+        store_bf16x32(dZ + jc, nv, v);
+      }
+    }
+  } else if constexpr (K == GemmKind::DGRAD_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
+    const size_t base = static_cast<size_t>(m) * 2 * p.F + static_cast<size_t>(i) * 2 * p.Fs;
+    const __nv_bfloat16* GU = p.aux + base;
+    __nv_bfloat16* dGU = static_cast<__nv_bfloat16*>(p.out0) + base;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int jc = j0 + c * 32;
+      if (jc >= p.Fs) break;
+      float da[32];
+      tmem_load_f32x32(tacc + c * 32, da);
+      const int nv = min(32, p.Fs - jc);
+      if (row_ok) {
+        float g[32], u[32];
+        load_bf16x32(GU + jc, nv, g);
+        load_bf16x32(GU + p.Fs + jc, nv, u);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float s = sigmoid_f(g[e]);
+          const float dg = da[e] * u[e] * s * (1.0f + g[e] * (1.0f - s));
+          u[e] = da[e] * g[e] * s;  // dU
+          g[e] = dg;                // dG
+        }
+        store_bf16x32(dGU + jc, nv, g);
+        store_bf16x32(dGU + p.Fs + jc, nv, u);
+      }
+    }
+  } else if constexpr (K == GemmKind::WGRAD_W2) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
+    float* dW = static_cast<float*>(p.out0) + (static_cast<size_t>(i) * p.H + m) * p.Fs;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int jc = j0 + c * 32;
+      if (jc >= p.Fs) break;
+      float v[32];
+      tmem_load_f32x32(tacc + c * 32, v);
+      if (row_ok) store_f32x32(dW + jc, min(32, p.Fs - jc), v);
+    }
+  } else {  // WGRAD_W1
+    const int n0 = nt * kBN;
+    float* dW = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= p.H) break;
+      float v[32];
+      tmem_load_f32x32(tacc + c * 32, v);
+      if (row_ok) store_f32x32(dW + col, min(32, p.H - col), v);
+    }
+  }
+}
+
+template <GemmKind K>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + kStages * kAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtx wc{abort_flag, p.err, p.wait_ns};
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool skip_once = p.fault_inject != 0 && blockIdx.x == 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, p, mt, nt);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (skip_once) {
+            skip_once = false;  // fault injection: this stage is never armed
+          } else {
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            issue_stage<K>(&tmA, &tmB, sA0 + stage * kAStage, sB0 + stage * kBStage, fb, mt, nt,
+                           kb, p);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Every copy this thread issued must land before the CTA exits.
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) wait_drain(full0 + 8 * s, (armed_par >> s) & 1u, wc);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, KindOf<K>::a_mn, KindOf<K>::b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!wait_bounded(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sA0 + stage * kAStage;
+          const uint32_t sb = sB0 + stage * kBStage;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = KindOf<K>::a_mn ? sdesc_sw128(sa + kk * 2048, kChunk, 1024)
+                                                : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = KindOf<K>::b_mn ? sdesc_sw128(sb + kk * 2048, kChunk, 1024)
+                                                : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull0 + 8 * buf);
+      }
+      // Drain: every MMA issued above has completed once this commit arrives.
+      umma_commit(drain);
+      wait_drain(drain, 0, wc);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull0 + 8 * buf, acc_par, wc, kSiteEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after();
+      int mt, nt;
+      tile_coords(tile, p, mt, nt);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
+      epilogue_tile<K>(tacc, row, mt, nt, p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace mlpb

@@ -1,0 +1,47 @@
+// Tile shapes, kinds and launch parameters of the tcgen05 GEMM (shared by host and device).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace mlpb {
+
+enum class GemmKind : int {
+  FC1_GELU = 0,
+  FC1_SWIGLU,
+  FC2,
+  DGRAD_GELU,
+  DGRAD_SWIGLU,
+  DX,
+  WGRAD_W2,
+  WGRAD_W1,
+};
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kAStage = kBM * kBK * 2;  // 16 KB
+constexpr int kBStage = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x 64(K) MN-major box, 8 KB
+constexpr int kGemmThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 + 256;
+
+struct GemmParams {
+  int num_m_tiles, num_n_tiles, num_kb;
+  int kb_per_shard;     // FC2: ceil(Fs / 64)
+  int tiles_per_shard;  // FC1_SWIGLU: ceil(Fs/128); DGRAD_*, WGRAD_W2: ceil(Fs/256)
+  int M;                // valid output rows
+  int T, H, F, Fs, t;
+  const __nv_bfloat16* bias;  // FC1_GELU: b1; FC2: b2 (nullable)
+  const __nv_bfloat16* aux;   // DGRAD_*: saved Z or G|U
+  void* out0;
+  void* out1;
+  uint32_t* err;
+  uint64_t wait_ns;
+  int fault_inject;
+};
+
+}  // namespace mlpb

@@ -1,0 +1,37 @@
+// Host-side launch functions of the library's kernels (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "gemm_params.h"
+
+namespace mlpb {
+
+// gemm_fwd.cu / gemm_bwd.cu: one persistent launch of the tcgen05 GEMM of `kind`.
+cudaError_t gemm_fwd_set_smem_attrs();
+cudaError_t gemm_bwd_set_smem_attrs();
+cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t s);
+
+// reduce.cu: column sums of a [R][C] bf16 matrix into fp32, deterministic two passes.
+//   pass 1: part[split][C] over row splits of `rows_per_split` rows; pass 2: out[C].
+cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
+                               int64_t rows_per_split, float* part, float* out, cudaStream_t s);
+cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
+                                cudaStream_t s);
+cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
+
+// layernorm.cu
+cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Xn,
+                          float* mean, float* rstd, int64_t T, int64_t H, float eps,
+                          cudaStream_t s);
+cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
+                          const float* dXn, float* dX, float* part_dg, float* part_db,
+                          int64_t T, int64_t H, int shards, int blocks_per_shard,
+                          cudaStream_t s);
+
+}  // namespace mlpb

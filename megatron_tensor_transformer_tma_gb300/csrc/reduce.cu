@@ -1,0 +1,108 @@
+// Bias-gradient column reductions (db2 = sum_t dY, db1 = sum_t dZ) and helpers.
+//
+// Pass 1: a CTA of 256 threads owns 512 columns x one split of rows; each thread keeps
+// 8 fp32 column sums (one 16-byte bf16 vector per row) over every 4th row of the split,
+// and the 4 row lanes are combined through shared memory into part[split][col].
+// Pass 2 sums the splits in a fixed order, so results are bitwise reproducible.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mlpb {
+
+constexpr int kColsPerCta = 512;
+constexpr int kRowLanes = 4;
+
+__global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                          int64_t R, int64_t C,
+                                                          int64_t rows_per_split,
+                                                          float* __restrict__ part) {
+  __shared__ float red[kRowLanes - 1][64][9];
+  const int cv = threadIdx.x & 63;
+  const int rl = threadIdx.x >> 6;
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * kColsPerCta + cv * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_split;
+  const int64_t r1 = min(R, r0 + rows_per_split);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (col < C) {
+    const __nv_bfloat16* p = in + col;
+    int64_t r = r0 + rl;
+#pragma unroll 4
+    for (; r < r1; r += kRowLanes) {
+      const uint4 u = ld_global_nc_v4(p + r * C);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
+    }
+  }
+  if (rl > 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[rl - 1][cv][e] = acc[e];
+  }
+  __syncthreads();
+  if (rl == 0 && col < C) {
+#pragma unroll
+    for (int l = 0; l < kRowLanes - 1; ++l)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += red[l][cv][e];
+    float* o = part + static_cast<int64_t>(blockIdx.y) * C + col;
+    st_global_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                               __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+    st_global_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                   __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+  }
+}
+
+// out[c] = sum_{k < nparts} part[k][c], summed in increasing k.
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ part,
+                                                           int nparts, int64_t C,
+                                                           float* __restrict__ out) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  float s = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < nparts; ++k) s += part[static_cast<int64_t>(k) * C + c];
+  out[c] = s;
+}
+
+__global__ void fill_zero_kernel(uint4* p, size_t n16, uint8_t* tail, size_t ntail) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0, 0, 0, 0);
+  if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0;
+}
+
+cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
+                               int64_t rows_per_split, float* part, float* out, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((C + kColsPerCta - 1) / kColsPerCta),
+                  static_cast<unsigned>(splits));
+  colsum_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), R, C,
+                                           rows_per_split, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_sum_partials(part, splits, C, out, s);
+}
+
+cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
+                                cudaStream_t s) {
+  const unsigned blocks = static_cast<unsigned>((C + 255) / 256);
+  sum_partials_kernel<<<blocks, 256, 0, s>>>(part, nparts, C, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  const size_t n16 = bytes / 16;
+  const size_t ntail = bytes - n16 * 16;
+  const unsigned blocks = static_cast<unsigned>(n16 / 256 + 1 < 4096 ? n16 / 256 + 1 : 4096);
+  fill_zero_kernel<<<blocks, 256, 0, s>>>(static_cast<uint4*>(p), n16,
+                                          static_cast<uint8_t*>(p) + n16 * 16, ntail);
+  return cudaGetLastError();
+}
+
+}  // namespace mlpb

@@ -1,0 +1,76 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the header
+declares, and rejects bad configurations before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import megatron_tensor_transformer_tma_gb300 as mlpb
+from megatron_tensor_transformer_tma_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mlpb.load_library()
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "mlpb.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlpb_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _header_functions()
+    assert len(declared) >= 12
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(mlpb.EXPORTED) == declared
+
+
+def test_status_strings(lib):
+    for code in range(0, -6, -1):
+        assert mlpb.status_str(code) not in ("", "unknown status")
+    assert mlpb.status_str(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(tokens=100), mlpb.MLPB_EUNSUPPORTED),          # T % 128
+    (dict(hidden=96), mlpb.MLPB_EUNSUPPORTED),           # H % 64
+    (dict(ffn=1000, tp=3), mlpb.MLPB_EUNSUPPORTED),      # F % t
+    (dict(ffn=1028, tp=2), mlpb.MLPB_EUNSUPPORTED),      # (F/t) % 8
+    (dict(act="swiglu", has_bias=True), mlpb.MLPB_EUNSUPPORTED),
+    (dict(tokens=256, tp=3, ffn=768, seq_parallel_ln=True), mlpb.MLPB_EUNSUPPORTED),
+    (dict(tp=0), mlpb.MLPB_EINVAL),
+    (dict(hidden=0), mlpb.MLPB_EINVAL),
+    (dict(tokens=-128), mlpb.MLPB_EINVAL),
+    (dict(flags=0x80), mlpb.MLPB_EINVAL),
+    (dict(seq_parallel_ln=True, ln_eps=0.0), mlpb.MLPB_EINVAL),
+])
+def test_create_rejects_bad_configs(lib, kw, status):
+    args = dict(tokens=128, hidden=256, ffn=1024, tp=2, act="gelu", has_bias=True)
+    args.update(kw)
+    cfg = mlpb.make_config(**args)
+    h = ctypes.c_void_p()
+    assert lib.mlpb_create(ctypes.byref(cfg), ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.mlpb_create(None, ctypes.byref(h)) == mlpb.MLPB_EINVAL
+    n = ctypes.c_size_t()
+    assert lib.mlpb_workspace_size(None, ctypes.byref(n)) == mlpb.MLPB_EINVAL
+    assert lib.mlpb_forward(None, *([None] * 10)) == mlpb.MLPB_EINVAL
+    assert lib.mlpb_backward(None, *([None] * 13)) == mlpb.MLPB_EINVAL
+    lib.mlpb_destroy(None)
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        mlpb.mlpb._ptr(torch.zeros(4), name="X")

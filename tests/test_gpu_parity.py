@@ -1,0 +1,136 @@
+"""GPU parity of the C-ABI path against the fp64 oracle (element by element).
+
+Shapes span several 128 x 256 tiles and ragged tails: Fs not a multiple of 64 or 128
+(shard seams inside a K block and inside an N tile), H = 64 mod 128 (a ragged M tile in
+the dW2 GEMM and a ragged N tile in fc2 / dX), t = 1 and t = 8, with and without bias,
+GELU and SwiGLU, and the sequence-parallel pre-LN block.
+"""
+import numpy as np
+import pytest
+import torch
+
+import megatron_tensor_transformer_tma_gb300 as mlpb
+from inputs import MLPShape, WORKLOADS, make_inputs, make_ln_grad
+from oracle import layernorm as oln
+
+from _harness import check_full, compare, oracle_full, run_gpu, to_f64
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    pytest.param(WORKLOADS[1], 1, id="tiny-gelu-t2"),
+    pytest.param(MLPShape(256, 512, 2048, 4, "gelu", True), 11, id="gelu-t4-multitile"),
+    pytest.param(MLPShape(384, 320, 1536, 1, "gelu", False), 12, id="gelu-t1-nobias-raggedH"),
+    pytest.param(MLPShape(256, 192, 704, 8, "swiglu", False), 13, id="swiglu-t8-Fs88-raggedH"),
+    pytest.param(MLPShape(512, 256, 2752, 2, "swiglu", False), 14, id="swiglu-t2-Fs1376"),
+    pytest.param(MLPShape(256, 256, 1024, 8, "gelu", True), 15, id="gelu-t8-Fs128"),
+    pytest.param(MLPShape(256, 384, 1024, 4, "swiglu", False, sp_ln=True), 16, id="sp-ln-swiglu-t4"),
+    pytest.param(MLPShape(128, 128, 512, 2, "gelu", True, sp_ln=True), 17, id="sp-ln-gelu-t2"),
+]
+
+
+@pytest.mark.parametrize("shape,wid", SMALL)
+def test_small_shapes_every_element(shape, wid):
+    d = make_inputs(shape, wid)
+    gpu = run_gpu(shape, d)
+    check_full(shape, gpu, oracle_full(shape, d))
+
+
+@pytest.mark.parametrize("tp", [1, 4])
+def test_gelu_h1024_f4096_full(tp):
+    shape = WORKLOADS[2].with_tp(tp)
+    d = make_inputs(shape, 2)
+    gpu = run_gpu(shape, d)
+    check_full(shape, gpu, oracle_full(shape, d))
+
+
+def test_deterministic_bitwise():
+    shape = MLPShape(256, 320, 1408, 4, "gelu", True)
+    d = make_inputs(shape, 21)
+    a = run_gpu(shape, d)
+    b = run_gpu(shape, d)
+    for k in ("Y", "dX", "dW1", "dW2", "db1", "db2"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_layernorm_sp_components():
+    """K8 / K9 alone on seeded inputs (the upstream dXn is seeded, not produced here)."""
+    shape = MLPShape(1024, 8192, 64, 8, "swiglu", False, sp_ln=True)
+    d = make_inputs(shape, 31)
+    dXn = make_ln_grad(shape, 31)
+    dev = torch.device("cuda:0")
+    h = mlpb.mlpb_create(mlpb.make_config(1024, 8192, 64, 8, "swiglu", False, True, 1e-5))
+    X, gm, bt = d["X"].to(dev), d["gamma"].to(dev), d["beta"].to(dev)
+    Xn = torch.empty_like(X)
+    mean = torch.empty(1024, device=dev)
+    rstd = torch.empty(1024, device=dev)
+    mlpb.mlpb_layernorm_sp_fwd(h, X, gm, bt, Xn, mean, rstd)
+    ws = torch.empty(mlpb.mlpb_workspace_size(h), dtype=torch.uint8, device=dev)
+    dX = torch.empty((1024, 8192), device=dev)
+    dg = torch.empty(8192, device=dev)
+    db = torch.empty(8192, device=dev)
+    mlpb.mlpb_layernorm_sp_bwd(h, X, gm, mean, rstd, dXn.to(dev), dX, dg, db, ws)
+    torch.cuda.synchronize()
+    assert mlpb.mlpb_last_device_error(h) == 0
+    mlpb.mlpb_destroy(h)
+    x64, g64, b64 = to_f64(d["X"]), to_f64(d["gamma"]), to_f64(d["beta"])
+    rXn, rmu, rrs = oln.layernorm_sp_fwd(x64, g64, b64, 1e-5, 8)
+    # Xn is bf16: within one bf16 rounding of the oracle plus 1e-3 RMS
+    got = to_f64(Xn)
+    assert np.all(np.abs(got - rXn) <= np.abs(rXn) * 2.0 ** -8 + 1e-3 * np.sqrt(np.mean(rXn ** 2)))
+    compare("mean", to_f64(mean), rmu, tol=1e-5)
+    compare("rstd", to_f64(rstd), rrs, tol=1e-5)
+    rdX, rdg, rdb = oln.layernorm_sp_bwd(x64, g64, rmu, rrs, to_f64(dXn), 8)
+    compare("ln_dX", to_f64(dX), rdX, tol=1e-4)
+    compare("dgamma", to_f64(dg), rdg, tol=1e-4)
+    compare("dbeta", to_f64(db), rdb, tol=1e-4)
+
+
+def test_empty_batch_zero_grads():
+    shape = MLPShape(0, 256, 1024, 2, "gelu", True)
+    d = make_inputs(MLPShape(128, 256, 1024, 2, "gelu", True), 41)
+    dev = torch.device("cuda:0")
+    blk = mlpb.MLPBlock(0, 256, 1024, 2, "gelu", True)
+    X = torch.empty((0, 256), dtype=torch.bfloat16, device=dev)
+    W1, W2 = d["W1"].to(dev), d["W2"].to(dev)
+    Y = blk.forward(X, W1, d["b1"].to(dev), W2, d["b2"].to(dev))
+    g = blk.alloc_grads(W1, W2)
+    for v in g.values():
+        v.fill_(7.0)
+    blk.backward(X, W1, W2, torch.empty((0, 256), dtype=torch.bfloat16, device=dev), g)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, 256)
+    for k in ("dW1", "dW2", "db1", "db2"):
+        assert torch.count_nonzero(g[k]).item() == 0, k
+    blk.close()
+    del shape
+
+
+def test_host_validation_launches_nothing():
+    dev = torch.device("cuda:0")
+    blk = mlpb.MLPBlock(128, 256, 1024, 2, "gelu", True)
+    X = torch.zeros((128 * 256 + 1,), dtype=torch.bfloat16, device=dev)[1:].view(128, 256)
+    W1 = torch.zeros((2, 512, 256), dtype=torch.bfloat16, device=dev)
+    W2 = torch.zeros((2, 256, 512), dtype=torch.bfloat16, device=dev)
+    b1 = torch.zeros(1024, dtype=torch.bfloat16, device=dev)
+    b2 = torch.zeros(256, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(mlpb.MLPBError) as e:
+        blk.forward(X, W1, b1, W2, b2)  # X misaligned by 2 bytes
+    assert e.value.status == mlpb.MLPB_EINVAL
+    with pytest.raises(mlpb.MLPBError) as e:
+        blk.forward(X.clone(), W1, None, W2, b2)  # bias config without b1
+    assert e.value.status == mlpb.MLPB_EINVAL
+    assert mlpb.mlpb_last_device_error(blk.handle) == 0
+    blk.close()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The producer skips one arrive (a flag nothing else sets); the consumer's bounded
+    wait expires, the kernel drains, frees tensor memory and returns; the host reads
+    MLPB_ETIMEOUT, and the next call on a fresh handle is correct."""
+    shape = WORKLOADS[1]
+    d = make_inputs(shape, 1)
+    bad = run_gpu(shape, d, flags=mlpb.MLPB_FLAG_FAULT_INJECT)
+    assert bad["status"] == mlpb.MLPB_ETIMEOUT
+    good = run_gpu(shape, d)
+    check_full(shape, good, oracle_full(shape, d))
