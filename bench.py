@@ -1,0 +1,425 @@
+"""Throughput of the tensor-parallel MLP block (forward + backward) on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input through
+the C ABI: [SP-LayerNorm forward] -> mlpb_forward (fc1 + fused activation, fc2 with
+the in-accumulator g all-reduce) -> mlpb_backward (db2, dgrad + act', db1, dW2, dW1,
+dX with the in-accumulator f all-reduce) -> [SP-LayerNorm backward].
+
+The metric is MLP-block fwd+bwd TFLOP/s (bf16 inputs, fp32 accumulation): the six
+GEMMs' algorithmic flops over the step time, and its fraction of the measured dense
+bf16 peak.  `value` times inputs resident in HBM; `e2e` times the same step with the
+inputs copied from pinned host memory and every output copied back, each step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl reference]
+
+N > 1 runs under torchrun as independent data-parallel replicas (the block has no
+exchange between GPUs on this path); `value` sums all ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLP-block fwd+bwd TFLOP/s (bf16) on 1 GB300 and fraction of dense bf16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["gemm.cuh", "gemm_params.h", "ptx.cuh", "common.cuh", "gemm_fwd.cu",
+                  "gemm_bwd.cu", "reduce.cu", "layernorm.cu"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--tp", type=int, default=None, help="override the emulated TP degree")
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "megatron_tensor_transformer_tma_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def config_of(shape, wid):
+    return {"workload": shape.name or f"workload {wid}", "tokens": shape.tokens,
+            "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
+            "activation": shape.act, "bias": shape.bias, "sp_layernorm": shape.sp_ln,
+            "parallelism": "emulated TP inside one GPU; replicas across GPUs",
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_step_fn(shape, wid, tokens):
+    """One fwd+bwd of the fp64 oracle on the first `tokens` rows of the workload."""
+    import numpy as np  # noqa: F401
+    from inputs import make_inputs
+    from oracle import layernorm as oln
+    from oracle import mlp as omlp
+    small = shape.with_tokens(tokens)
+    d = make_inputs(small, wid)
+    f = {k: (v.double().numpy() if v is not None else None) for k, v in d.items()}
+
+    def step():
+        if shape.sp_ln:
+            oln.block_forward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
+                              f["W2"], f["b2"], shape.act, shape.tp)
+            oln.block_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
+                               f["W2"], f["dY"], shape.act, shape.tp)
+        else:
+            omlp.mlp_forward(f["X"], f["W1"], f["b1"], f["W2"], f["b2"], shape.act)
+            omlp.mlp_backward(f["X"], f["W1"], f["b1"], f["W2"], f["dY"], shape.act)
+    return step, small.gemm_flops()
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(shape, wid, target_s):
+    """The oracle as it stands, timed on this host's cores on a bounded token sample."""
+    tokens = 128
+    step, flops = oracle_step_fn(shape, wid, tokens)
+    t0 = time.perf_counter()
+    step()
+    dt = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(dt, 1e-3)))
+    if reps > 4 and shape.tokens >= 1024:  # prefer one larger sample to many small ones
+        tokens = min(shape.tokens, 128 * min(8, reps // 2))
+        step, flops = oracle_step_fn(shape, wid, tokens)
+        t0 = time.perf_counter()
+        step()
+        dt = time.perf_counter() - t0
+        reps = max(1, int(target_s / max(dt, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        step()
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} x fwd+bwd of the fp64 oracle on the first {tokens} of "
+                      f"{shape.tokens} tokens (same H, F, t); numpy BLAS on all host cores"}
+
+
+def run_reference(args, rank, world):
+    from inputs import workload
+    if rank != 0:
+        return
+    shape = workload(args.workload, args.tp)
+    step, flops = oracle_step_fn(shape, args.workload, 128)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = flops / dt / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": config_of(shape, args.workload),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                            "sample": f"each step: fwd+bwd of the fp64 oracle on the first 128 "
+                                      f"of {shape.tokens} tokens"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(dev):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return dev.index or 0
+
+
+# ------------------------------------------------------------------ native leg
+def run_native(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import megatron_tensor_transformer_tma_gb300 as mlpb
+    from inputs import make_inputs, workload
+
+    shape = workload(args.workload, args.tp)
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    # the oracle baseline runs first, before any GPU work, on rank 0 at N = 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, args.workload, args.cpu_seconds)
+
+    d = make_inputs(shape, args.workload)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    blk = mlpb.MLPBlock(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act, shape.bias,
+                        shape.sp_ln, shape.ln_eps)
+    grads = blk.alloc_grads(g["W1"], g["W2"])
+    T, H = shape.tokens, shape.hidden
+    Y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if shape.sp_ln:
+        Xn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        mean = torch.empty((T,), dtype=torch.float32, device=dev)
+        rstd = torch.empty((T,), dtype=torch.float32, device=dev)
+        dXin = torch.empty((T, H), dtype=torch.float32, device=dev)
+        dgamma = torch.empty((H,), dtype=torch.float32, device=dev)
+        dbeta = torch.empty((H,), dtype=torch.float32, device=dev)
+    h = blk.handle
+
+    def step(src):
+        X = src["X"]
+        if shape.sp_ln:
+            mlpb.mlpb_layernorm_sp_fwd(h, X, src["gamma"], src["beta"], Xn, mean, rstd)
+            X = Xn
+        blk.forward(X, src["W1"], src["b1"], src["W2"], src["b2"], Y)
+        blk.backward(X, src["W1"], src["W2"], src["dY"], grads)
+        if shape.sp_ln:
+            mlpb.mlpb_layernorm_sp_bwd(h, src["X"], src["gamma"], mean, rstd, grads["dX"], dXin,
+                                       dgamma, dbeta, blk.workspace)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step(g)
+    barrier()
+    assert mlpb.mlpb_last_device_error(h) == 0, "device error during warm-up"
+
+    # ---- timed region: inputs resident in HBM
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(gpu_smi_id(dev))
+    time.sleep(0.2)
+    mlpb.mlpb_enable_timing(h, True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(g)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    recs = mlpb.mlpb_read_timings(h, capacity=64 * max(args.steps, 1))
+    mlpb.mlpb_enable_timing(h, False)
+    assert mlpb.mlpb_last_device_error(h) == 0, "device error during the timed steps"
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops_step = shape.gemm_flops()
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    # ---- per-kernel aggregation (CUDA events around each launch, same stream)
+    per = {}
+    for r in recs:
+        k = per.setdefault(r["name"], {"ms": 0.0, "launches": 0, "flops": r["flops"],
+                                       "bytes": r["bytes"], "kernels": 0})
+        k["ms"] += r["ms"]
+        k["launches"] += 1
+        k["kernels"] += r["kernels"]
+    gpu_launches = sum(k["kernels"] for k in per.values())
+    peaks, peak_src = load_peaks()
+    kernels = []
+    for name, k in sorted(per.items(), key=lambda kv: -kv[1]["ms"]):
+        avg = k["ms"] / k["launches"]
+        row = {"name": name, "launches": k["launches"], "avg_ms": avg,
+               "share": k["ms"] / sum(v["ms"] for v in per.values())}
+        if k["flops"] > 0:
+            row["tflops"] = k["flops"] / (avg * 1e-3) / 1e12
+        if k["bytes"] > 0:
+            row["gbs"] = k["bytes"] / (avg * 1e-3) / 1e9
+        kernels.append(row)
+    top = kernels[0]
+    topk = per[top["name"]]
+    if topk["flops"] > 0:
+        achieved = topk["flops"] / (top["avg_ms"] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": top["name"], "achieved": achieved,
+                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "peak_source": f"{peak_src} sustained dense bf16 (kernel timed inside a long step)"}
+    else:
+        achieved = topk["bytes"] / (top["avg_ms"] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": top["name"], "achieved": achieved,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"{peak_src} copy"}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["traffic"] = recorded_traffic(top["name"], args.workload, shape)
+
+    # ---- e2e: the same step from pinned host buffers, outputs read back every step
+    e2e = run_e2e(args, shape, d, blk, step, grads, Y, dev, world)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+               "config": config_of(shape, args.workload),
+               "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
+               "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
+               "roofline": roofline, "kernels": kernels, "gpu_launches": gpu_launches,
+               "e2e": e2e, "clocks": clk, "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+    blk.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def recorded_traffic(kernel, wid, shape):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this kernel,
+    this workload and the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        recs = json.load(f)
+    cur = kernel_source_hash()
+    for r in recs:
+        if r.get("kernel") == kernel and r.get("workload") == wid and r.get("source_hash") == cur:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+def run_e2e(args, shape, d, blk, step, grads, Y, dev, world):
+    import torch
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in d.items()}
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None)
+              for k, v in d.items()}
+    outs = {"Y": Y, **{k: v for k, v in grads.items() if v is not None}}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k, v in pinned.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        step(dev_in)
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    n = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": shape.gemm_flops() * world / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "api": "mlpb_forward + mlpb_backward via the ctypes binding"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and "WORLD_SIZE" in os.environ:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    run_native(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -38,6 +38,8 @@
  *       Y, dX               [T][H] fp32
  *       dW1, dW2            fp32 in the layouts of W1, W2;  db1 [F], db2 [H] fp32
  *     where T = tokens, H = hidden, F = ffn, t = tp, Fs = F / t.
+ *   - With T = 0 the activation pointers (X, Y, Z/A saved, dY, dX, workspace) may be
+ *     NULL; the forward does nothing and the backward writes zero weight/bias grads.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  Argument errors are returned synchronously and launch
  *     nothing.  Outputs are overwritten, never accumulated into.
@@ -72,8 +74,6 @@ typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
 #define MLPB_FLAG_FAULT_INJECT 0x1u    /* test only: the first GEMM launch of the  \
                                           next forward skips one producer arrive, so \
                                           its consumers' bounded wait expires        */
-#define MLPB_FLAG_EMULATE_COPIES 0x2u  /* SP gather / reduce-scatter run as explicit \
-                                          in-device copy kernels (costs bandwidth)   */
 
 typedef struct {
   int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */
@@ -95,6 +95,8 @@ typedef struct {
   float ms;       /* device time between CUDA events recorded around the launch   */
   double flops;   /* algorithmic GEMM flops of the launch (0 for memory kernels)  */
   double bytes;   /* algorithmic HBM bytes of the launch (minimum reads + writes) */
+  int32_t kernels; /* CUDA kernels launched inside this record (e.g. 2 for a       \
+                      two-pass reduction)                                          */
 } mlpb_kernel_time;
 
 /* Validates *cfg, queries the current device and allocates the 4-byte device

@@ -21,6 +21,7 @@ namespace {
 struct TimedLaunch {
   char name[32];
   double flops, bytes;
+  int kernels;
   cudaEvent_t start, stop;
 };
 
@@ -112,12 +113,14 @@ struct LaunchTimer {
   mlpb_handle* h;
   cudaStream_t s;
   TimedLaunch rec{};
-  LaunchTimer(mlpb_handle* h_, cudaStream_t s_, const char* name, double flops, double bytes)
+  LaunchTimer(mlpb_handle* h_, cudaStream_t s_, const char* name, double flops, double bytes,
+              int kernels = 1)
       : h(h_), s(s_) {
     if (!h->timing) return;
     std::snprintf(rec.name, sizeof(rec.name), "%s", name);
     rec.flops = flops;
     rec.bytes = bytes;
+    rec.kernels = kernels;
     rec.start = h->take_event();
     rec.stop = h->take_event();
     cudaEventRecord(rec.start, s);
@@ -292,7 +295,8 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
   (void)workspace;
   if (h == nullptr) return MLPB_EINVAL;
   const bool bias = h->cfg.has_bias != 0;
-  if (!X || !W1 || !W2 || !Y || !Zsaved || !Asaved) return MLPB_EINVAL;
+  if (!W1 || !W2) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !Y || !Zsaved || !Asaved)) return MLPB_EINVAL;  // T = 0: empty tensors
   if (bias != (b1 != nullptr) || bias != (b2 != nullptr)) return MLPB_EINVAL;
   for (const void* p : {X, W1, W2, static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
                         static_cast<const void*>(Asaved), b1, b2})
@@ -365,8 +369,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
                           mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;
   const bool bias = h->cfg.has_bias != 0;
-  if (!X || !W1 || !W2 || !Zsaved || !Asaved || !dY || !dX || !dW1 || !dW2 || !workspace)
-    return MLPB_EINVAL;
+  if (!W1 || !W2 || !dW1 || !dW2) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !Zsaved || !Asaved || !dY || !dX || !workspace))
+    return MLPB_EINVAL;  // T = 0: the activation tensors are empty
   if (bias != (db1 != nullptr) || bias != (db2 != nullptr)) return MLPB_EINVAL;
   for (const void* p : {X, W1, W2, Zsaved, Asaved, dY, static_cast<const void*>(dX),
                         static_cast<const void*>(dW1), static_cast<const void*>(dW2),
@@ -393,7 +398,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H);
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
     cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
@@ -424,7 +429,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db1 = sum_t dZ
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F);
+    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
     cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
@@ -523,7 +528,7 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
                                 h->ln_blocks_per_shard, s);
   lt.done();
   if (e == cudaSuccess) {
-    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H);
+    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H, 2);
     e = launch_sum_partials(pg, nblk, H, dgamma, s);
     if (e == cudaSuccess) e = launch_sum_partials(pb, nblk, H, dbeta, s);
     lt2.done();
@@ -565,6 +570,7 @@ mlpb_status mlpb_read_timings(mlpb_handle* h, mlpb_kernel_time* out, int capacit
       out[n].ms = ms;
       out[n].flops = l.flops;
       out[n].bytes = l.bytes;
+      out[n].kernels = l.kernels;
       ++n;
     }
     h->event_pool.push_back(l.start);

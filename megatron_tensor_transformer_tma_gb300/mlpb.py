@@ -45,7 +45,7 @@ class mlpb_config(ctypes.Structure):
 
 class mlpb_kernel_time(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("ms", ctypes.c_float), ("flops", ctypes.c_double),
-                ("bytes", ctypes.c_double)]
+                ("bytes", ctypes.c_double), ("kernels", ctypes.c_int32)]
 
 
 class MLPBError(RuntimeError):
@@ -240,7 +240,7 @@ def mlpb_read_timings(h: Handle, capacity: int = 64):
     _check(load_library().mlpb_read_timings(h.ptr, buf, capacity, ctypes.byref(n)),
            "mlpb_read_timings")
     return [dict(name=buf[i].name.decode(), ms=buf[i].ms, flops=buf[i].flops,
-                 bytes=buf[i].bytes) for i in range(n.value)]
+                 bytes=buf[i].bytes, kernels=buf[i].kernels) for i in range(n.value)]
 
 
 class MLPBlock:

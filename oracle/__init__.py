@@ -6,4 +6,4 @@ and ``bench.py``'s CPU-baseline leg.  The library never imports it, and it
 imports nothing from the library.  Parity status of every function is pinned
 by ``tests/test_oracle_pins.py`` (see the design notes for the list of pins).
 """
-from . import mlp, layernorm  # noqa: F401
+from . import bf16, mlp, layernorm  # noqa: F401

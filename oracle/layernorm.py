@@ -87,16 +87,21 @@ def layernorm_sp_bwd(X, gamma, mean, rstd, dXn, t):
 
 
 # ---------------------------------------------------------------- pre-LN block, Y = MLP(LN(X))
-def block_forward(X, gamma, beta, eps, W1, b1, W2, b2, act, t):
+# ``store`` (default exact) is applied to the LN output, which the block keeps as
+# fc1's and dW1's GEMM input, and passed on to the MLP (see ``mlp.mlp_forward``).
+def block_forward(X, gamma, beta, eps, W1, b1, W2, b2, act, t, store=None):
+    S = store or _mlp._identity
     Xn, mu, rstd = layernorm_fwd(X, gamma, beta, eps)
-    out = _mlp.mlp_forward(Xn, W1, b1, W2, b2, act)
+    Xn = S(Xn)
+    out = _mlp.mlp_forward(Xn, W1, b1, W2, b2, act, store)
     out.update(Xn=Xn, mean=mu, rstd=rstd)
     return out
 
 
-def block_backward(X, gamma, beta, eps, W1, b1, W2, dY, act, t):
+def block_backward(X, gamma, beta, eps, W1, b1, W2, dY, act, t, store=None):
+    S = store or _mlp._identity
     Xn, mu, rstd = layernorm_fwd(X, gamma, beta, eps)
-    g = _mlp.mlp_backward(Xn, W1, b1, W2, dY, act)
+    g = _mlp.mlp_backward(S(Xn), W1, b1, W2, dY, act, store)
     dX, dgamma, dbeta = layernorm_bwd(X, gamma, mu, rstd, g["dX"])
     g.update(dXn=g["dX"], dX=dX, dgamma=dgamma, dbeta=dbeta)
     return g
@@ -165,17 +170,19 @@ def block_sp_forward_backward(X, gamma, beta, eps, W1, b1, W2, b2, dY, act, t):
             "dgamma": dgamma, "dbeta": dbeta}
 
 
-def block_rows(X, gamma, beta, eps, W1, b1, W2, b2, dY, rows, act):
+def block_rows(X, gamma, beta, eps, W1, b1, W2, b2, dY, rows, act, store=None):
     """Y[rows] and dX[rows] of the pre-LN block (row-separable end to end)."""
+    S = store or _mlp._identity
     rows = np.asarray(rows)
     Xr = _f64(X)[rows]
     Xn, mu, rstd = layernorm_fwd(Xr, gamma, beta, eps)
-    r = _mlp.mlp_rows(Xn, W1, b1, W2, b2, _f64(dY)[rows], np.arange(len(rows)), act)
+    r = _mlp.mlp_rows(S(Xn), W1, b1, W2, b2, _f64(dY)[rows], np.arange(len(rows)), act, store)
     dX, _, _ = layernorm_bwd(Xr, gamma, mu, rstd, r["dX"])
     return {"Y": r["Y"], "dXn": r["dX"], "dX": dX}
 
 
-def block_ffn_cols(X, gamma, beta, eps, W1, b1, W2, dY, cols, act):
+def block_ffn_cols(X, gamma, beta, eps, W1, b1, W2, dY, cols, act, store=None):
     """Sampled ffn-feature gradients of the pre-LN block (fc1 sees LN(X))."""
+    S = store or _mlp._identity
     Xn, _, _ = layernorm_fwd(X, gamma, beta, eps)
-    return _mlp.mlp_ffn_cols(Xn, W1, b1, W2, dY, cols, act)
+    return _mlp.mlp_ffn_cols(S(Xn), W1, b1, W2, dY, cols, act, store)

@@ -143,11 +143,14 @@ def _f64(a):
 
 
 # ---------------------------------------------------------------- plain (unsharded) path
-def mlp_forward(X, W1, b1, W2, b2, act="gelu"):
+def mlp_forward(X, W1, b1, W2, b2, act="gelu", store=None):
     """Unsharded forward.  Returns Y and the saved activations.
 
     GELU -> {"Y", "Z", "A"};  SwiGLU -> {"Y", "G", "U", "A"} (b1, b2 unused/None).
+    ``store`` (default: exact) is applied to every activation the block keeps as a
+    GEMM input -- A, and the saved Z or G, U -- e.g. ``bf16.round_bf16``.
     """
+    S = store or _identity
     X, b1, b2 = _f64(X), _f64(b1), _f64(b2)
     W2f = full_w2(W2)
     out = {}
@@ -155,16 +158,16 @@ def mlp_forward(X, W1, b1, W2, b2, act="gelu"):
         Wg, Wu = full_w1(W1, act)
         G = X @ Wg.T
         U = X @ Wu.T
-        A = silu(G) * U
-        out.update(G=G, U=U)
+        A = S(silu(G) * U)
+        out.update(G=S(G), U=S(U))
     else:
         fn, _ = _POINTWISE[act]
         W1f = full_w1(W1, act)
         Z = X @ W1f.T
         if b1 is not None:
             Z = Z + b1
-        A = fn(Z)
-        out["Z"] = Z
+        A = S(fn(Z))
+        out["Z"] = S(Z)
     Y = A @ W2f.T
     if b2 is not None:
         Y = Y + b2
@@ -172,15 +175,17 @@ def mlp_forward(X, W1, b1, W2, b2, act="gelu"):
     return out
 
 
-def mlp_backward(X, W1, b1, W2, dY, act="gelu"):
+def mlp_backward(X, W1, b1, W2, dY, act="gelu", store=None):
     """Unsharded backward (recomputes the forward activations itself).
 
     Returns dX [T, H], dW1 (shard-major like W1), dW2 [t, H, Fs], db1 [F] (or
-    None without bias), db2 [H].
+    None without bias), db2 [H].  With ``store``, the derivative uses the stored
+    Z (or G, U), dW2 the stored A, and dZ is stored before its three uses.
     """
+    S = store or _identity
     X, b1, dY = _f64(X), _f64(b1), _f64(dY)
     t = np.asarray(W2).shape[0]
-    fwd = mlp_forward(X, W1, b1, W2, None, act)
+    fwd = mlp_forward(X, W1, b1, W2, None, act, store)
     A = fwd["A"]
     W2f = full_w2(W2)
     db2 = dY.sum(axis=0)
@@ -189,15 +194,15 @@ def mlp_backward(X, W1, b1, W2, dY, act="gelu"):
     if act == "swiglu":
         Wg, Wu = full_w1(W1, act)
         G, U = fwd["G"], fwd["U"]
-        dG = dA * U * silu_grad(G)
-        dU = dA * silu(G)
+        dG = S(dA * U * silu_grad(G))
+        dU = S(dA * silu(G))
         dX = dG @ Wg + dU @ Wu
         dW1 = shard_w1_grad((dG.T @ X, dU.T @ X), t, act)
         db1 = None
     else:
         _, dfn = _POINTWISE[act]
         W1f = full_w1(W1, act)
-        dZ = dA * dfn(fwd["Z"])
+        dZ = S(dA * dfn(fwd["Z"]))
         dX = dZ @ W1f
         dW1 = shard_w1_grad(dZ.T @ X, t, act)
         db1 = dZ.sum(axis=0) if b1 is not None else None
@@ -282,17 +287,17 @@ def mlp_backward_sharded(X, W1, b1, W2, dY, act="gelu"):
 
 
 # ---------------------------------------------------------------- sampled outputs
-def mlp_rows(X, W1, b1, W2, b2, dY, rows, act="gelu"):
+def mlp_rows(X, W1, b1, W2, b2, dY, rows, act="gelu", store=None):
     """Y[rows] and dX[rows]: every output row depends only on its own input row."""
     rows = np.asarray(rows)
     Xr = _f64(X)[rows]
     dYr = _f64(dY)[rows]
-    fwd = mlp_forward(Xr, W1, b1, W2, b2, act)
-    bwd = mlp_backward(Xr, W1, b1, W2, dYr, act)
+    fwd = mlp_forward(Xr, W1, b1, W2, b2, act, store)
+    bwd = mlp_backward(Xr, W1, b1, W2, dYr, act, store)
     return {"Y": fwd["Y"], "dX": bwd["dX"]}
 
 
-def mlp_ffn_cols(X, W1, b1, W2, dY, cols, act="gelu"):
+def mlp_ffn_cols(X, W1, b1, W2, dY, cols, act="gelu", store=None):
     """Gradients of the sampled ffn features f (over all T tokens).
 
     Returns dW1_rows (GELU: [n, H]; SwiGLU: [n, 2, H] gate then up),
@@ -300,6 +305,7 @@ def mlp_ffn_cols(X, W1, b1, W2, dY, cols, act="gelu"):
     db1 [n] or None.  Feature f depends only on row f of W1 (gate and up),
     column f of W2 and entry f of b1.
     """
+    S = store or _identity
     cols = np.asarray(cols)
     X, dY, b1 = _f64(X), _f64(dY), _f64(b1)
     W2f = full_w2(W2)[:, cols]                          # [H, n]
@@ -308,9 +314,10 @@ def mlp_ffn_cols(X, W1, b1, W2, dY, cols, act="gelu"):
         Wg, Wu = full_w1(W1, act)
         G = X @ Wg[cols].T
         U = X @ Wu[cols].T
-        A = silu(G) * U
-        dG = dA * U * silu_grad(G)
-        dU = dA * silu(G)
+        A = S(silu(G) * U)
+        G, U = S(G), S(U)
+        dG = S(dA * U * silu_grad(G))
+        dU = S(dA * silu(G))
         dW1 = np.stack([dG.T @ X, dU.T @ X], axis=1)
         db1 = None
     else:
@@ -319,8 +326,8 @@ def mlp_ffn_cols(X, W1, b1, W2, dY, cols, act="gelu"):
         Z = X @ W1f[cols].T
         if b1 is not None:
             Z = Z + b1[cols]
-        A = fn(Z)
-        dZ = dA * dfn(Z)
+        A = S(fn(Z))
+        dZ = S(dA * dfn(S(Z)))
         dW1 = dZ.T @ X
         db1 = dZ.sum(axis=0) if b1 is not None else None
     dW2 = (dY.T @ A).T                                  # [n, H]

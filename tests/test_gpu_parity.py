@@ -13,7 +13,7 @@ import megatron_tensor_transformer_tma_gb300 as mlpb
 from inputs import MLPShape, WORKLOADS, make_inputs, make_ln_grad
 from oracle import layernorm as oln
 
-from _harness import check_full, compare, oracle_full, run_gpu, to_f64
+from _harness import check_full, compare, oracle_pair, run_gpu, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ SMALL = [
 def test_small_shapes_every_element(shape, wid):
     d = make_inputs(shape, wid)
     gpu = run_gpu(shape, d)
-    check_full(shape, gpu, oracle_full(shape, d))
+    check_full(shape, gpu, oracle_pair(shape, d))
 
 
 @pytest.mark.parametrize("tp", [1, 4])
@@ -41,7 +41,7 @@ def test_gelu_h1024_f4096_full(tp):
     shape = WORKLOADS[2].with_tp(tp)
     d = make_inputs(shape, 2)
     gpu = run_gpu(shape, d)
-    check_full(shape, gpu, oracle_full(shape, d))
+    check_full(shape, gpu, oracle_pair(shape, d))
 
 
 def test_deterministic_bitwise():
@@ -133,4 +133,4 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     bad = run_gpu(shape, d, flags=mlpb.MLPB_FLAG_FAULT_INJECT)
     assert bad["status"] == mlpb.MLPB_ETIMEOUT
     good = run_gpu(shape, d)
-    check_full(shape, good, oracle_full(shape, d))
+    check_full(shape, good, oracle_pair(shape, d))

@@ -398,3 +398,56 @@ def test_planted_mistake_is_caught(monkeypatch, target, attr, mutant):
     if attr == "gelu_tanh":
         monkeypatch.setitem(mlp._POINTWISE, "gelu", (mutant, mlp.gelu_tanh_grad))
     assert not _all_pins_pass()
+
+
+# ------------------------------------------------------------------ bf16 storage reading
+def test_round_bf16_matches_torch_conversion():
+    """Pinned to torch's own float32 -> bfloat16 conversion (round to nearest even)."""
+    import torch
+    from oracle.bf16 import round_bf16
+    r = np.random.default_rng(5)
+    x32 = np.concatenate([
+        r.standard_normal(200000).astype(np.float32) * np.float32(10.0) ** r.integers(-30, 30, 200000).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.0e38, 1e-39, -2.5e-40], dtype=np.float32),
+    ])
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = round_bf16(x32.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_round_bf16_ties_to_even_and_idempotent():
+    from oracle.bf16 import round_bf16
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties go to the even significand (1)
+    assert round_bf16(1.0 + 2.0 ** -8) == 1.0
+    assert round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    x = np.random.default_rng(6).standard_normal(10000)
+    once = round_bf16(x)
+    assert np.array_equal(round_bf16(once), once)
+    assert np.all(np.abs(once - x) <= np.abs(x) * 2.0 ** -8)
+
+
+@pytest.mark.parametrize("act,bias", [("gelu", True), ("swiglu", False)])
+def test_store_hook_and_sampled_modes_agree(act, bias):
+    from oracle.bf16 import identity, round_bf16
+    t = 2
+    d = _mlp_inputs(16, 16, 32, t, act, bias, seed=61)
+    a = mlp.mlp_backward(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], act)
+    b = mlp.mlp_backward(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], act, identity)
+    for k in ("dX", "dW1", "dW2"):
+        assert np.array_equal(a[k], b[k])
+    full_b = mlp.mlp_backward(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], act, round_bf16)
+    full_f = mlp.mlp_forward(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], act, round_bf16)
+    rows = np.array([0, 9, 15])
+    r = mlp.mlp_rows(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], d["dY"], rows, act, round_bf16)
+    assert _rel(r["Y"], full_f["Y"][rows]) < 1e-13 and _rel(r["dX"], full_b["dX"][rows]) < 1e-13
+    cols = np.array([0, 15, 16, 31])
+    c = mlp.mlp_ffn_cols(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], cols, act, round_bf16)
+    for n, f in enumerate(cols):
+        i, j = divmod(int(f), 16)
+        assert _rel(c["dW2"][n], full_b["dW2"][i, :, j]) < 1e-13
+        want = full_b["dW1"][i, :, j] if act == "swiglu" else full_b["dW1"][i, j]
+        assert _rel(c["dW1"][n], want) < 1e-13
+    # the stored activations really are bf16 values
+    assert np.array_equal(round_bf16(full_f["A"]), full_f["A"])
+    # and the rounded result stays within a few bf16 units of the exact one
+    assert _rel(full_f["Y"], mlp.mlp_forward(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], act)["Y"]) < 2e-2
