@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     p.add_argument("--tp", type=int, default=None, help="override the emulated TP degree")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the token count (smaller cases for profiling)")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -133,11 +135,16 @@ def cpu_baseline(shape, wid, target_s):
                       f"{shape.tokens} tokens (same H, F, t); numpy BLAS on all host cores"}
 
 
-def run_reference(args, rank, world):
+def bench_shape(args):
     from inputs import workload
+    shape = workload(args.workload, args.tp)
+    return shape if args.tokens is None else shape.with_tokens(args.tokens)
+
+
+def run_reference(args, rank, world):
     if rank != 0:
         return
-    shape = workload(args.workload, args.tp)
+    shape = bench_shape(args)
     step, flops = oracle_step_fn(shape, args.workload, 128)
     for _ in range(args.warmup):
         step()
@@ -223,9 +230,9 @@ def run_native(args, rank, world, local_rank):
     import torch.distributed as dist
 
     import megatron_tensor_transformer_tma_gb300 as mlpb
-    from inputs import make_inputs, workload
+    from inputs import make_inputs
 
-    shape = workload(args.workload, args.tp)
+    shape = bench_shape(args)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if world > 1:
