@@ -169,6 +169,23 @@ mlpb_status mlpb_enable_timing(mlpb_handle *h, int enable);
  * (waiting on their events), sets *count, and clears the list. */
 mlpb_status mlpb_read_timings(mlpb_handle *h, mlpb_kernel_time *out, int capacity, int *count);
 
+/* Column sums out[c] = sum_r in[r][c] of a bf16 [rows][cols] matrix into fp32 -- the
+ * bias-gradient reduction of mlpb_backward (db2 = sum_t dY, db1 = sum_t dZ) -- for
+ * callers that cannot allocate device memory where they need it (code under a memory
+ * manager that owns all of the GPU's memory, or inside that manager's own callbacks).
+ * The pages have no counterpart: this is an allocation-free variant of the same kernels.
+ * It needs no handle and no workspace: its scratch is a fixed 4 MiB device array inside
+ * the library (held by every GPU that loads the library until the process exits).
+ * The first call on a device looks up that array's device address and the SM count
+ * (once per device, with the device current); make that first call before any stream
+ * capture.  Every call shares the one array: calls whose kernels overlap on the GPU
+ * (other streams, other host threads) race on it and must be serialised by the caller.
+ * Requires cols % 8 == 0 and cols <= 1048576 (one split of fp32 partials must fit the
+ * scratch; larger widths return MLPB_EUNSUPPORTED), 16-byte aligned `in` and `out`;
+ * rows may be 0 (out becomes zeros, `in` may then be NULL).  Allocates nothing. */
+mlpb_status mlpb_bias_grad_noalloc(const void *in, int64_t rows, int64_t cols, float *out,
+                                   mlpb_stream_t stream);
+
 /* Static English text of a status code. */
 const char *mlpb_status_str(mlpb_status s);
 

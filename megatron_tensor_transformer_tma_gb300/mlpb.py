@@ -31,7 +31,7 @@ MLPB_FLAG_FAULT_INJECT = 0x1
 EXPORTED = (
     "mlpb_create", "mlpb_destroy", "mlpb_workspace_size", "mlpb_saved_size", "mlpb_forward",
     "mlpb_backward", "mlpb_layernorm_sp_fwd", "mlpb_layernorm_sp_bwd", "mlpb_last_device_error",
-    "mlpb_enable_timing", "mlpb_read_timings", "mlpb_status_str",
+    "mlpb_enable_timing", "mlpb_read_timings", "mlpb_status_str", "mlpb_bias_grad_noalloc",
 )
 
 
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mlpb_enable_timing": (I, [H, I]),
         "mlpb_read_timings": (I, [H, ctypes.POINTER(mlpb_kernel_time), I, ctypes.POINTER(I)]),
         "mlpb_status_str": (ctypes.c_char_p, [I]),
+        "mlpb_bias_grad_noalloc": (I, [P, ctypes.c_int64, ctypes.c_int64, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -241,6 +242,16 @@ def mlpb_read_timings(h: Handle, capacity: int = 64):
            "mlpb_read_timings")
     return [dict(name=buf[i].name.decode(), ms=buf[i].ms, flops=buf[i].flops,
                  bytes=buf[i].bytes, kernels=buf[i].kernels) for i in range(n.value)]
+
+
+def mlpb_bias_grad_noalloc(inp, out, stream=None):
+    """Column sums of a bf16 [rows][cols] CUDA tensor into the fp32 [cols] tensor `out`,
+    with no device allocation (the library's fixed scratch array; see include/mlpb.h)."""
+    rows, cols = inp.shape
+    args = [_ptr(inp, torch.bfloat16, None, "in"), rows, cols,
+            _ptr(out, torch.float32, (cols,), "out")]
+    _check(load_library().mlpb_bias_grad_noalloc(*args, _stream(stream)),
+           "mlpb_bias_grad_noalloc")
 
 
 class MLPBlock:
