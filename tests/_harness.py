@@ -63,13 +63,19 @@ def gate(name, got, exact, stored, tol=TOL):
 
 
 def compare_stored(name, got, ref):
-    """bf16 activations: within one bf16 unit (2^-7 relative) of the bf16-storage
-    oracle, plus 1e-3 RMS for fp32-vs-fp64 accumulation order."""
+    """bf16 activations against the bf16-storage oracle: within one bf16 unit (2^-7
+    relative) plus 1e-3 RMS, except for at most 1e-6 of the entries (where the GPU's
+    fp32 and the oracle's fp64 inputs to a rounding straddle a bf16 boundary upstream),
+    and every entry within two units plus 1e-2 RMS."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape and np.isfinite(got).all(), name
     rms = float(np.sqrt(np.mean(ref * ref)))
-    bad = np.abs(got - ref) > np.abs(ref) * 2.0 ** -7 + 1e-3 * rms
-    assert not bad.any(), f"{name}: {int(bad.sum())} entries beyond one bf16 unit"
+    diff = np.abs(got - ref)
+    near = int((diff > np.abs(ref) * 2.0 ** -7 + 1e-3 * rms).sum())
+    assert near <= max(1, int(1e-6 * ref.size)), f"{name}: {near} entries beyond one bf16 unit"
+    far = int((diff > np.abs(ref) * 2.0 ** -6 + 1e-2 * rms).sum())
+    assert far == 0, f"{name}: {far} entries beyond two bf16 units + 1e-2 RMS"
 
 
 def pack_glu(G, U, t):
