@@ -496,7 +496,8 @@ mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle* h, const void* X, const void* gam
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t T = h->T, H = h->H;
   LaunchTimer lt(h, s, "ln_fwd", 0.0, 4.0 * T * H + 8.0 * T + 4.0 * H);
-  cudaError_t e = launch_ln_fwd(X, gamma, beta, Xn, mean, rstd, T, H, h->cfg.ln_eps, s);
+  cudaError_t e = launch_ln_fwd(X, gamma, beta, Xn, mean, rstd, T, H, h->cfg.ln_eps,
+                                h->num_sms, h->d_err, h->wait_ns, s);
   lt.done();
   return from_cuda(e);
 }
@@ -525,12 +526,11 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
   }
   LaunchTimer lt(h, s, "ln_bwd", 0.0, 10.0 * T * H + 8.0 * T + 10.0 * H);
   cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dX, pg, pb, T, H, h->t,
-                                h->ln_blocks_per_shard, s);
+                                h->ln_blocks_per_shard, h->d_err, h->wait_ns, s);
   lt.done();
   if (e == cudaSuccess) {
-    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H, 2);
-    e = launch_sum_partials(pg, nblk, H, dgamma, s);
-    if (e == cudaSuccess) e = launch_sum_partials(pb, nblk, H, dbeta, s);
+    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H, 1);
+    e = launch_sum_partials2(pg, pb, nblk, H, dgamma, dbeta, s);
     lt2.done();
   }
   return from_cuda(e);

@@ -17,6 +17,7 @@ enum WaitSite : uint32_t {
   kSiteMmaAccEmpty = 3,
   kSiteEpiAccFull = 4,
   kSiteDrain = 5,
+  kSiteLnFull = 6,
 };
 
 // Default limit of one bounded wait: 1 s of wall time (globaltimer).

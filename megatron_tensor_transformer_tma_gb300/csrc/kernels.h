@@ -23,15 +23,19 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int64_t rows_per_split, float* part, float* out, cudaStream_t s);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s);
+// Two [nparts][C] partial arrays summed into two outputs in one launch.
+cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
+                                 float* out_a, float* out_b, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 
-// layernorm.cu
+// layernorm.cu: rows streamed through a shared-memory ring by TMA bulk copies; bounded
+// waits report to `err`.
 cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Xn,
-                          float* mean, float* rstd, int64_t T, int64_t H, float eps,
-                          cudaStream_t s);
+                          float* mean, float* rstd, int64_t T, int64_t H, float eps, int num_sms,
+                          uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
                           const float* dXn, float* dX, float* part_dg, float* part_db,
-                          int64_t T, int64_t H, int shards, int blocks_per_shard,
-                          cudaStream_t s);
+                          int64_t T, int64_t H, int shards, int blocks_per_shard, uint32_t* err,
+                          uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace mlpb

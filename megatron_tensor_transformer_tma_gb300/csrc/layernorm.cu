@@ -1,28 +1,35 @@
 // Sequence-parallel LayerNorm forward and backward.
 //
-// Forward: one CTA per row, ceil(H/16) threads (a multiple of 32, at most 1024); each
-// thread keeps two 16-byte bf16 vectors of the row in registers, so mean and variance are
-// two passes over registers (warp shuffles, then one value per warp through shared
-// memory).  Sequence shard s owns rows [s T/t, (s+1) T/t); rows are independent, so the
-// shard structure only matters for the parameter gradients.
+// Both kernels stream whole rows into a ring of shared-memory buffers with TMA bulk
+// copies (cp.async.bulk), so the next rows' loads stay in flight while the CTA reduces
+// and writes the current one.  256 threads per CTA; thread i owns the 16-byte vectors
+// i, i+256, ... of the row (kVpt vectors), so every global store is coalesced.
+//
+// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row the mean and
+// the biased variance are two passes over the register-resident row (warp shuffles, then
+// one value per warp through shared memory); Xn = (x - mu) rstd gamma + beta in bf16.
+// Sequence shard s owns rows [s T/t, (s+1) T/t); rows are independent, so the forward
+// needs no shard structure and the emulated all-gather is the row layout of Xn itself.
 //
 // Backward: a grid of t x B CTAs; CTA (s, b) walks rows b, b+B, ... of shard s, computes
 // dx = rstd (g - mean(g) - xhat mean(g xhat)) with g = dy gamma, and accumulates its own
-// dgamma/dbeta partials in registers.  The partials [t*B][H] are then summed in shard
-// order (the all-reduce of per-shard partials), deterministically.
+// dgamma/dbeta partials in registers.  The partials [t*B][H] are summed afterwards in
+// shard order (the all-reduce of per-shard partials), deterministically.
+//
+// Every mbarrier wait is bounded; a CTA that gives up records the device error word,
+// waits for the copies it issued and exits.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mlpb {
 
-// kLnVpt: 16-byte vectors (8 elements) per thread; 2 for H <= 8192, 4 for H <= 16384,
-// with at most 512 threads per CTA.
-constexpr int kLnMaxThreads = 512;
+constexpr int kLnThreads = 256;
 
 template <int NV>
-__device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [32*NV] */) {
+__device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [8*NV] */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
 #pragma unroll
   for (int k = 0; k < NV; ++k)
 #pragma unroll
@@ -35,7 +42,8 @@ __device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [32*NV] *
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     float s = 0.f;
-    for (int w = 0; w < nwarps; ++w) s += sh[w * NV + k];
+#pragma unroll
+    for (int w = 0; w < kLnThreads / 32; ++w) s += sh[w * NV + k];
     v[k] = s;
   }
 }
@@ -50,96 +58,193 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-template <int kLnVpt>
-__global__ void __launch_bounds__(kLnMaxThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ X,
-                                                      const __nv_bfloat16* __restrict__ gamma,
-                                                      const __nv_bfloat16* __restrict__ beta,
-                                                      __nv_bfloat16* __restrict__ Xn,
-                                                      float* __restrict__ mean,
-                                                      float* __restrict__ rstd, int H,
-                                                      float eps) {
-  __shared__ float sh[32];
-  const int64_t row = blockIdx.x;
-  const __nv_bfloat16* x = X + row * H;
-  float v[kLnVpt][8];
-  bool ok[kLnVpt];
-  float s[1] = {0.f};
-#pragma unroll
-  for (int k = 0; k < kLnVpt; ++k) {
-    const int c = (threadIdx.x + k * blockDim.x) * 8;
-    ok[k] = c < H;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (ok[k]) u = ld_global_nc_v4(x + c);
-    bf16x8_to_f32(u, v[k]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s[0] += v[k][e];
-  }
-  block_sum<1>(s, sh);
-  const float mu = s[0] / static_cast<float>(H);
-  float q[1] = {0.f};
-#pragma unroll
-  for (int k = 0; k < kLnVpt; ++k)
-    if (ok[k])
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float d = v[k][e] - mu;
-        q[0] += d * d;
-      }
-  block_sum<1>(q, sh);
-  const float r = rsqrtf(q[0] / static_cast<float>(H) + eps);
-#pragma unroll
-  for (int k = 0; k < kLnVpt; ++k) {
-    if (!ok[k]) continue;
-    const int c = (threadIdx.x + k * blockDim.x) * 8;
-    float g[8], b[8], o[8];
-    bf16x8_to_f32(ld_global_nc_v4(gamma + c), g);
-    bf16x8_to_f32(ld_global_nc_v4(beta + c), b);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mu) * r * g[e] + b[e];
-    st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                                              pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
-  }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_f32x8(float* p, const float* o) {
+  st_global_v4(p, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                             __float_as_uint(o[3])));
+  st_global_v4(p + 4, make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]),
+                                 __float_as_uint(o[6]), __float_as_uint(o[7])));
+}
+
+// ------------------------------------------------------------------ forward
+template <int kVpt>
+__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
+    const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ Xn,
+    float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
+    uint32_t* err, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float sh[8];
+  __shared__ uint32_t abort_flag;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
+  const uint32_t buf0 = smem_u32(smem);
+  const uint32_t bar0 = buf0 + nbuf * row_bytes;
+  const int64_t n_mine = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const WaitCtx wc{&abort_flag, err, wait_ns};
+
   if (threadIdx.x == 0) {
-    mean[row] = mu;
-    rstd[row] = r;
+    abort_flag = 0u;
+    for (int b = 0; b < nbuf; ++b) mbar_init(bar0 + 8 * b, 1);
+    mbar_fence_init();
+    for (int b = 0; b < nbuf && b < n_mine; ++b) {
+      const int64_t row = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
+      bulk_load(buf0 + b * row_bytes, X + row * H, row_bytes, bar0 + 8 * b);
+    }
+  }
+  __syncthreads();
+
+  float gm[kVpt][8], bt[kVpt][8];
+  bool ok_v[kVpt];
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int c = (threadIdx.x + k * kLnThreads) * 8;
+    ok_v[k] = c < H;
+    uint4 g = make_uint4(0, 0, 0, 0), b = g;
+    if (ok_v[k]) {
+      g = ld_global_nc_v4(gamma + c);
+      b = ld_global_nc_v4(beta + c);
+    }
+    bf16x8_to_f32(g, gm[k]);
+    bf16x8_to_f32(b, bt[k]);
+  }
+
+  int64_t issued = nbuf < n_mine ? nbuf : n_mine;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int b = static_cast<int>(i % nbuf);
+    const uint32_t par = static_cast<uint32_t>((i / nbuf) & 1);
+    int ok = wait_bounded(bar0 + 8 * b, par, wc, kSiteLnFull) ? 1 : 0;
+    if (!__syncthreads_and(ok)) break;
+    const int64_t row = blockIdx.x + i * gridDim.x;
+    float v[kVpt][8];
+    float s[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k) {
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (ok_v[k]) u = ld_shared_v4(buf0 + b * row_bytes + (threadIdx.x + k * kLnThreads) * 16);
+      bf16x8_to_f32(u, v[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s[0] += v[k][e];
+    }
+    block_sum<1>(s, sh);  // every thread has read buffer b once this returns
+    if (threadIdx.x == 0 && issued < n_mine) {
+      const int64_t nrow = blockIdx.x + issued * gridDim.x;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
+      bulk_load(buf0 + b * row_bytes, X + nrow * H, row_bytes, bar0 + 8 * b);
+    }
+    ++issued;
+    const float mu = s[0] / static_cast<float>(H);
+    float q[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k)
+      if (ok_v[k])
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = v[k][e] - mu;
+          q[0] += d * d;
+        }
+    block_sum<1>(q, sh);
+    const float r = rsqrtf(q[0] / static_cast<float>(H) + eps);
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k) {
+      if (!ok_v[k]) continue;
+      const int c = (threadIdx.x + k * kLnThreads) * 8;
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mu) * r * gm[k][e] + bt[k][e];
+      st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                                pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
+    }
+    if (threadIdx.x == 0) {
+      mean[row] = mu;
+      rstd[row] = r;
+    }
+  }
+  // Copies still in flight (only after an abort) must land before the CTA exits.
+  if (threadIdx.x == 0 && abort_flag) {
+    const int64_t first = issued - nbuf > 0 ? issued - nbuf : 0;
+    for (int64_t i = first; i < issued && i < n_mine; ++i)
+      wait_drain(bar0 + 8 * static_cast<int>(i % nbuf), static_cast<uint32_t>((i / nbuf) & 1), wc);
   }
 }
 
-template <int kLnVpt>
-__global__ void __launch_bounds__(kLnMaxThreads) ln_bwd_kernel(
+// ------------------------------------------------------------------ backward
+template <int kVpt>
+__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
     const float* __restrict__ mean, const float* __restrict__ rstd,
     const float* __restrict__ dXn, float* __restrict__ dX, float* __restrict__ part_dg,
-    float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H) {
-  __shared__ float sh[64];
+    float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H, int nbuf,
+    uint32_t* err, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float sh[16];
+  __shared__ uint32_t abort_flag;
+  const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * 6u;  // X bf16 then dXn fp32
+  const uint32_t buf0 = smem_u32(smem);
+  const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int shard = blockIdx.x / blocks_per_shard;
-  const int b = blockIdx.x - shard * blocks_per_shard;
-  float gm[kLnVpt][8], adg[kLnVpt][8], adb[kLnVpt][8];
-  bool ok[kLnVpt];
+  const int bidx = blockIdx.x - shard * blocks_per_shard;
+  const int64_t rbeg = shard * rows_per_shard;
+  const int64_t n_mine =
+      bidx < rows_per_shard ? (rows_per_shard - bidx + blocks_per_shard - 1) / blocks_per_shard : 0;
+  const WaitCtx wc{&abort_flag, err, wait_ns};
+
+  auto issue = [&](int b, int64_t i) {
+    const int64_t row = rbeg + bidx + i * blocks_per_shard;
+    mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
+    bulk_load(buf0 + b * row_bytes, X + row * H, xbytes, bar0 + 8 * b);
+    bulk_load(buf0 + b * row_bytes + xbytes, dXn + row * H, 4u * H, bar0 + 8 * b);
+  };
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    for (int b = 0; b < nbuf; ++b) mbar_init(bar0 + 8 * b, 1);
+    mbar_fence_init();
+    for (int b = 0; b < nbuf && b < n_mine; ++b) issue(b, b);
+  }
+  __syncthreads();
+
+  float gm[kVpt][8], adg[kVpt][8], adb[kVpt][8];
+  bool ok_v[kVpt];
 #pragma unroll
-  for (int k = 0; k < kLnVpt; ++k) {
-    const int c = (threadIdx.x + k * blockDim.x) * 8;
-    ok[k] = c < H;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (ok[k]) u = ld_global_nc_v4(gamma + c);
-    bf16x8_to_f32(u, gm[k]);
+  for (int k = 0; k < kVpt; ++k) {
+    const int c = (threadIdx.x + k * kLnThreads) * 8;
+    ok_v[k] = c < H;
+    uint4 g = make_uint4(0, 0, 0, 0);
+    if (ok_v[k]) g = ld_global_nc_v4(gamma + c);
+    bf16x8_to_f32(g, gm[k]);
 #pragma unroll
     for (int e = 0; e < 8; ++e) adg[k][e] = adb[k][e] = 0.f;
   }
-  const int64_t rbeg = shard * rows_per_shard;
-  for (int64_t lr = b; lr < rows_per_shard; lr += blocks_per_shard) {
-    const int64_t row = rbeg + lr;
+
+  int64_t issued = nbuf < n_mine ? nbuf : n_mine;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int b = static_cast<int>(i % nbuf);
+    const uint32_t par = static_cast<uint32_t>((i / nbuf) & 1);
+    int ok = wait_bounded(bar0 + 8 * b, par, wc, kSiteLnFull) ? 1 : 0;
+    if (!__syncthreads_and(ok)) break;
+    const int64_t row = rbeg + bidx + i * blocks_per_shard;
     const float mu = mean[row], rs = rstd[row];
-    float xh[kLnVpt][8], g[kLnVpt][8], dy[kLnVpt][8];
+    const uint32_t xb = buf0 + b * row_bytes;
+    const uint32_t db = xb + xbytes;
+    float xh[kVpt][8], dy[kVpt][8];
     float s[2] = {0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < kLnVpt; ++k) {
-      const int c = (threadIdx.x + k * blockDim.x) * 8;
+    for (int k = 0; k < kVpt; ++k) {
+      const uint32_t vi = threadIdx.x + k * kLnThreads;
       uint4 ux = make_uint4(0, 0, 0, 0), d0 = ux, d1 = ux;
-      if (ok[k]) {
-        ux = ld_global_nc_v4(X + row * H + c);
-        d0 = ld_global_nc_v4(dXn + row * H + c);
-        d1 = ld_global_nc_v4(dXn + row * H + c + 4);
+      if (ok_v[k]) {
+        ux = ld_shared_v4(xb + vi * 16);
+        d0 = ld_shared_v4(db + vi * 32);
+        d1 = ld_shared_v4(db + vi * 32 + 16);
       }
       bf16x8_to_f32(ux, xh[k]);
       dy[k][0] = __uint_as_float(d0.x); dy[k][1] = __uint_as_float(d0.y);
@@ -148,88 +253,121 @@ __global__ void __launch_bounds__(kLnMaxThreads) ln_bwd_kernel(
       dy[k][6] = __uint_as_float(d1.z); dy[k][7] = __uint_as_float(d1.w);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        xh[k][e] = ok[k] ? (xh[k][e] - mu) * rs : 0.f;
-        g[k][e] = dy[k][e] * gm[k][e];
-        s[0] += g[k][e];
-        s[1] += g[k][e] * xh[k][e];
+        xh[k][e] = ok_v[k] ? (xh[k][e] - mu) * rs : 0.f;
+        const float g = dy[k][e] * gm[k][e];
+        s[0] += g;
+        s[1] += g * xh[k][e];
       }
     }
-    block_sum<2>(s, sh);
+    block_sum<2>(s, sh);  // every thread has read buffer b once this returns
+    if (threadIdx.x == 0 && issued < n_mine) {
+      fence_proxy_async_smem();
+      issue(b, issued);
+    }
+    ++issued;
     const float mg = s[0] / static_cast<float>(H);
     const float mgx = s[1] / static_cast<float>(H);
 #pragma unroll
-    for (int k = 0; k < kLnVpt; ++k) {
-      if (!ok[k]) continue;
-      const int c = (threadIdx.x + k * blockDim.x) * 8;
+    for (int k = 0; k < kVpt; ++k) {
+      if (!ok_v[k]) continue;
+      const int c = (threadIdx.x + k * kLnThreads) * 8;
       float o[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        o[e] = rs * (g[k][e] - mg - xh[k][e] * mgx);
+        o[e] = rs * (dy[k][e] * gm[k][e] - mg - xh[k][e] * mgx);
         adg[k][e] += dy[k][e] * xh[k][e];
         adb[k][e] += dy[k][e];
       }
-      float* d = dX + row * H + c;
-      st_global_v4(d, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]),
-                                 __float_as_uint(o[2]), __float_as_uint(o[3])));
-      st_global_v4(d + 4, make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]),
-                                     __float_as_uint(o[6]), __float_as_uint(o[7])));
+      st_f32x8(dX + row * H + c, o);
     }
   }
+  if (threadIdx.x == 0 && abort_flag) {
+    const int64_t first = issued - nbuf > 0 ? issued - nbuf : 0;
+    for (int64_t i = first; i < issued && i < n_mine; ++i)
+      wait_drain(bar0 + 8 * static_cast<int>(i % nbuf), static_cast<uint32_t>((i / nbuf) & 1), wc);
+  }
 #pragma unroll
-  for (int k = 0; k < kLnVpt; ++k) {
-    if (!ok[k]) continue;
-    const int c = (threadIdx.x + k * blockDim.x) * 8;
-    float* pg = part_dg + static_cast<int64_t>(blockIdx.x) * H + c;
-    float* pb = part_db + static_cast<int64_t>(blockIdx.x) * H + c;
-    st_global_v4(pg, make_uint4(__float_as_uint(adg[k][0]), __float_as_uint(adg[k][1]),
-                                __float_as_uint(adg[k][2]), __float_as_uint(adg[k][3])));
-    st_global_v4(pg + 4, make_uint4(__float_as_uint(adg[k][4]), __float_as_uint(adg[k][5]),
-                                    __float_as_uint(adg[k][6]), __float_as_uint(adg[k][7])));
-    st_global_v4(pb, make_uint4(__float_as_uint(adb[k][0]), __float_as_uint(adb[k][1]),
-                                __float_as_uint(adb[k][2]), __float_as_uint(adb[k][3])));
-    st_global_v4(pb + 4, make_uint4(__float_as_uint(adb[k][4]), __float_as_uint(adb[k][5]),
-                                    __float_as_uint(adb[k][6]), __float_as_uint(adb[k][7])));
+  for (int k = 0; k < kVpt; ++k) {
+    if (!ok_v[k]) continue;
+    const int c = (threadIdx.x + k * kLnThreads) * 8;
+    st_f32x8(part_dg + static_cast<int64_t>(blockIdx.x) * H + c, adg[k]);
+    st_f32x8(part_db + static_cast<int64_t>(blockIdx.x) * H + c, adb[k]);
   }
 }
 
-static unsigned ln_threads(int64_t H, int vpt) {
-  int64_t t = (H + 8 * vpt - 1) / (8 * vpt);
-  t = (t + 31) / 32 * 32;
-  return static_cast<unsigned>(t < 32 ? 32 : t);
+// ------------------------------------------------------------------ launchers
+static int ln_vpt(int64_t H) {
+  const int64_t v = (H / 8 + kLnThreads - 1) / kLnThreads;
+  return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : 8;
+}
+
+template <class K>
+static cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bytes));
 }
 
 cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Xn,
-                          float* mean, float* rstd, int64_t T, int64_t H, float eps,
-                          cudaStream_t s) {
+                          float* mean, float* rstd, int64_t T, int64_t H, float eps, int num_sms,
+                          uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  const size_t row = static_cast<size_t>(H) * 2;
+  int nbuf = static_cast<int>(std::min<size_t>(4, std::max<size_t>(2, (96u << 10) / row)));
+  const size_t smem = nbuf * row + 8 * nbuf;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(T, 2 * num_sms));
   const auto* x = static_cast<const __nv_bfloat16*>(X);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
   auto* xn = static_cast<__nv_bfloat16*>(Xn);
-  if (H <= 8192)
-    ln_fwd_kernel<2><<<static_cast<unsigned>(T), ln_threads(H, 2), 0, s>>>(
-        x, g, b, xn, mean, rstd, static_cast<int>(H), eps);
-  else
-    ln_fwd_kernel<4><<<static_cast<unsigned>(T), ln_threads(H, 4), 0, s>>>(
-        x, g, b, xn, mean, rstd, static_cast<int>(H), eps);
+  const int Hi = static_cast<int>(H);
+  cudaError_t e = cudaSuccess;
+  switch (ln_vpt(H)) {
+#define MLPB_LN_FWD(V)                                                                     \
+  case V:                                                                                  \
+    e = set_smem(ln_fwd_kernel<V>, smem);                                                  \
+    if (e == cudaSuccess)                                                                  \
+      ln_fwd_kernel<V><<<grid, kLnThreads, smem, s>>>(x, g, b, xn, mean, rstd, T, Hi, eps, \
+                                                      nbuf, err, wait_ns);                 \
+    break;
+    MLPB_LN_FWD(1)
+    MLPB_LN_FWD(2)
+    MLPB_LN_FWD(4)
+    MLPB_LN_FWD(8)
+#undef MLPB_LN_FWD
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
                           const float* dXn, float* dX, float* part_dg, float* part_db,
-                          int64_t T, int64_t H, int shards, int blocks_per_shard,
-                          cudaStream_t s) {
+                          int64_t T, int64_t H, int shards, int blocks_per_shard, uint32_t* err,
+                          uint64_t wait_ns, cudaStream_t s) {
+  const size_t row = static_cast<size_t>(H) * 6;
+  int nbuf = static_cast<int>(std::min<size_t>(4, std::max<size_t>(2, (160u << 10) / row)));
+  const size_t smem = nbuf * row + 8 * nbuf;
   const unsigned grid = static_cast<unsigned>(shards * blocks_per_shard);
   const auto* x = static_cast<const __nv_bfloat16*>(X);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
-  if (H <= 8192)
-    ln_bwd_kernel<2><<<grid, ln_threads(H, 2), 0, s>>>(x, g, mean, rstd, dXn, dX, part_dg,
-                                                       part_db, T / shards, blocks_per_shard,
-                                                       static_cast<int>(H));
-  else
-    ln_bwd_kernel<4><<<grid, ln_threads(H, 4), 0, s>>>(x, g, mean, rstd, dXn, dX, part_dg,
-                                                       part_db, T / shards, blocks_per_shard,
-                                                       static_cast<int>(H));
+  const int Hi = static_cast<int>(H);
+  const int64_t rps = T / shards;
+  cudaError_t e = cudaSuccess;
+  switch (ln_vpt(H)) {
+#define MLPB_LN_BWD(V)                                                                       \
+  case V:                                                                                    \
+    e = set_smem(ln_bwd_kernel<V>, smem);                                                    \
+    if (e == cudaSuccess)                                                                    \
+      ln_bwd_kernel<V><<<grid, kLnThreads, smem, s>>>(x, g, mean, rstd, dXn, dX, part_dg,    \
+                                                      part_db, rps, blocks_per_shard, Hi,    \
+                                                      nbuf, err, wait_ns);                   \
+    break;
+    MLPB_LN_BWD(1)
+    MLPB_LN_BWD(2)
+    MLPB_LN_BWD(4)
+    MLPB_LN_BWD(8)
+#undef MLPB_LN_BWD
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   if (col < C) {
     const __nv_bfloat16* p = in + col;
     int64_t r = r0 + rl;
-#pragma unroll 4
+#pragma unroll 8
     for (; r < r1; r += kRowLanes) {
       const uint4 u = ld_global_nc_v4(p + r * C);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -58,16 +58,31 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
-// out[c] = sum_{k < nparts} part[k][c], summed in increasing k.
-__global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ part,
-                                                           int nparts, int64_t C,
-                                                           float* __restrict__ out) {
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c >= C) return;
+// out[c] = sum_k part[k][c] for one or two partial arrays (blockIdx.y picks the array).
+// A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
+// eight warp sums are added in warp order -- a fixed order, so results are reproducible.
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float* part_a,
+                                                           const float* part_b, int nparts,
+                                                           int64_t C, float* out_a,
+                                                           float* out_b) {
+  __shared__ float red[8][33];
+  const float* part = blockIdx.y == 0 ? part_a : part_b;
+  float* out = blockIdx.y == 0 ? out_a : out_b;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float s = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < nparts; ++k) s += part[static_cast<int64_t>(k) * C + c];
-  out[c] = s;
+  if (c < C) {
+#pragma unroll 4
+    for (int k = warp; k < nparts; k += 8) s += part[static_cast<int64_t>(k) * C + c];
+  }
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && c < C) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w][lane];
+    out[c] = t;
+  }
 }
 
 __global__ void fill_zero_kernel(uint4* p, size_t n16, uint8_t* tail, size_t ntail) {
@@ -90,8 +105,15 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
 
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s) {
-  const unsigned blocks = static_cast<unsigned>((C + 255) / 256);
-  sum_partials_kernel<<<blocks, 256, 0, s>>>(part, nparts, C, out);
+  const dim3 grid(static_cast<unsigned>((C + 31) / 32), 1);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part, part, nparts, C, out, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
+                                 float* out_a, float* out_b, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((C + 31) / 32), 2);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, part_b, nparts, C, out_a, out_b);
   return cudaGetLastError();
 }
 
