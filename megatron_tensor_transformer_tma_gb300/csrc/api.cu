@@ -82,7 +82,9 @@ struct mlpb_handle {
   bool swiglu;
   int device;
   int num_sms;
-  uint32_t* d_err;
+  int max_clusters;  // co-resident GEMM clusters
+  uint32_t* d_err;            // [0]: device error word; [64..]: colsum chunk counters
+  unsigned int* d_counters;
   bool fault_pending;
   uint64_t wait_ns;
   // bias-grad split plans
@@ -150,13 +152,20 @@ GemmParams base_params(const mlpb_handle* h) {
 mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap& a,
                      const CUtensorMap& b, const GemmParams& p, cudaStream_t s, const char* name,
                      double flops, double bytes) {
-  const int tiles = p.num_m_tiles * p.num_n_tiles;
-  if (tiles == 0) return MLPB_OK;
-  const int grid = std::min(tiles, h->num_sms);
+  const int super_tiles = static_cast<int>(cdiv(p.num_m_tiles, kClusterM)) * p.num_n_tiles;
+  if (super_tiles == 0) return MLPB_OK;
+  const int clusters = std::min(super_tiles, h->max_clusters);
   LaunchTimer lt(h, s, name, flops, bytes);
-  cudaError_t e = fwd ? launch_gemm_fwd(kind, a, b, p, grid, s) : launch_gemm_bwd(kind, a, b, p, grid, s);
+  cudaError_t e = fwd ? launch_gemm_fwd(kind, a, b, p, clusters, s)
+                      : launch_gemm_bwd(kind, a, b, p, clusters, s);
   lt.done();
   return from_cuda(e);
+}
+
+// Error word plus one zeroed arrival counter per 512-column chunk of the widest column
+// sum (db1 over F or db2 over H).
+size_t kDevWordsBytes(const mlpb_handle* h) {
+  return (64 + static_cast<size_t>(cdiv(std::max(h->F, h->H), 512))) * sizeof(uint32_t);
 }
 
 size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
@@ -250,16 +259,23 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   }
   if (load_encoder() != MLPB_OK || gemm_fwd_set_smem_attrs() != cudaSuccess ||
       gemm_bwd_set_smem_attrs() != cudaSuccess ||
-      cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+      cudaMalloc(reinterpret_cast<void**>(&h->d_err), kDevWordsBytes(h)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, kDevWordsBytes(h)) != cudaSuccess) {
     if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return MLPB_ECUDA;
+  }
+  h->d_counters = reinterpret_cast<unsigned int*>(h->d_err + 64);
+  if (gemm_max_active_clusters(&h->max_clusters) != cudaSuccess || h->max_clusters < 1) {
+    cudaFree(h->d_err);
     delete h;
     return MLPB_ECUDA;
   }
   plan_colsum(h->T, h->H, h->num_sms, &h->db2_splits, &h->db2_rows);
   plan_colsum(h->T, h->F, h->num_sms, &h->db1_splits, &h->db1_rows);
+  // LN backward: two CTAs per SM, split evenly over the t sequence shards
   h->ln_blocks_per_shard =
-      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(h->num_sms, h->t),
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(2 * h->num_sms, h->t),
                                                                h->t ? h->T / h->t : 1)));
   *out = h;
   return MLPB_OK;
@@ -318,7 +334,7 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
   if (!map2d(&ta, X, H, T, H, kBK, kBM)) return MLPB_EINVAL;
   mlpb_status st;
   if (!h->swiglu) {
-    if (!map2d(&tb, W1, H, F, H, kBK, kBN)) return MLPB_EINVAL;
+    if (!map2d(&tb, W1, H, F, H, kBK, kBN / 2)) return MLPB_EINVAL;
     p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
     p.bias = static_cast<const __nv_bfloat16*>(b1);
     st = run_gemm(h, GemmKind::FC1_GELU, true, ta, tb, p, s, "fc1_gelu", 2.0 * T * F * H,
@@ -346,7 +362,7 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
     const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
-    const uint32_t bbox[3] = {kBK, kBN, 1};
+    const uint32_t bbox[3] = {kBK, kBN / 2, 1};
     if (!encode_bf16(&ta, Asaved, 3, adims, astr, abox) ||
         !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
       return MLPB_EINVAL;
@@ -398,8 +414,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
-    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s);
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 1);
+    cudaError_t e = launch_colsum_bf16_fused(dY, T, H, h->db2_splits, h->db2_rows, part2, db2,
+                                             h->d_counters, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
   }
@@ -429,8 +446,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db1 = sum_t dZ
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
-    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s);
+    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 1);
+    cudaError_t e = launch_colsum_bf16_fused(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1,
+                                             h->d_counters, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
   }

@@ -1,11 +1,15 @@
 // Persistent, warp-specialised tcgen05 GEMM for the MLP block's six contractions.
 //
-// One CTA per SM (192 threads):
+// One CTA per SM (192 threads), CTAs paired in clusters of CM = 2 along M: the two CTAs
+// of a pair compute M tiles 2p and 2p+1 against the same N tile, so each loads its own A
+// tile and HALF of the shared B tile, multicasting that half into both CTAs' shared
+// memory (a third fewer L2->SM bytes per CTA than loading B alone).
 //   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
 //               (128-byte swizzle) and arms the stage's mbarrier with the byte count;
 //   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
 //               N=256, K=16) from one thread into one of two 256-column fp32
-//               accumulators, committing each consumed stage back to the producer;
+//               accumulators, committing each consumed stage back to the producers of
+//               both CTAs of the pair (a stage is refilled only when both have read it);
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp owns the 32 TMEM lanes
 //               of its warp-id modulo 4), apply the fused pointwise op, store to HBM,
 //               then release the accumulator so the next tile's K loop can run.
@@ -37,60 +41,93 @@ struct KindOf {
                                 K == GemmKind::WGRAD_W1);
 };
 
-// Grouped rasterisation: 8 consecutive M tiles sweep all N tiles together so that the
-// B tiles they share stay in L2.
-__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& mt, int& nt) {
+// Grouped rasterisation: 8 consecutive M tiles (or M-tile pairs) sweep all N tiles
+// together so that the B tiles they share stay in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mt, int& nt) {
   constexpr int G = 8;
-  const int span = G * p.num_n_tiles;
+  const int span = G * num_n;
   const int g = tile / span;
   const int m0 = g * G;
-  const int gm = min(p.num_m_tiles - m0, G);
+  const int gm = min(num_m - m0, G);
   const int r = tile - g * span;
   mt = m0 + r % gm;
   nt = r / gm;
 }
 
-template <GemmKind K>
+// TMA loads that multicast to both CTAs of the pair when CM == 2.
+template <int CM>
+__device__ __forceinline__ void tma2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                     int c1) {
+  if constexpr (CM == 1) tma_load_2d(dst, m, bar, c0, c1);
+  else tma_load_2d_mc(dst, m, bar, c0, c1, static_cast<uint16_t>((1u << CM) - 1));
+}
+template <int CM>
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                     int c1, int c2) {
+  if constexpr (CM == 1) tma_load_3d(dst, m, bar, c0, c1, c2);
+  else tma_load_3d_mc(dst, m, bar, c0, c1, c2, static_cast<uint16_t>((1u << CM) - 1));
+}
+template <int CM>
+__device__ __forceinline__ void tma4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                     int c1, int c2, int c3) {
+  if constexpr (CM == 1) tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  else tma_load_4d_mc(dst, m, bar, c0, c1, c2, c3, static_cast<uint16_t>((1u << CM) - 1));
+}
+
+// One stage: this CTA's own A tile, and the B pieces this CTA owns.  B is two 128-row
+// K-major pieces (16 KB) or four 64-wide MN-major chunks (8 KB); with CM = 2 the CTA of
+// rank r loads pieces r (or chunks 2r, 2r+1) and multicasts them to both CTAs.
+template <GemmKind K, int CM>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tA, const CUtensorMap* tB,
                                             uint32_t sa, uint32_t sb, uint32_t bar, int mt,
-                                            int nt, int kb, const GemmParams& p) {
+                                            int nt, int kb, int rank, const GemmParams& p) {
   const int k0 = kb * kBK;
   if constexpr (K == GemmKind::FC1_GELU) {
     tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_2d(sb, tB, bar, k0, nt * kBN);
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma2<CM>(sb + q * (kBStage / 2), tB, bar, k0, nt * kBN + 128 * q);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * 128;
     tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_4d(sb, tB, bar, k0, j0, 0, i);            // gate rows -> B rows 0..127
-    tma_load_4d(sb + kBStage / 2, tB, bar, k0, j0, 1, i);  // up rows -> B rows 128..255
+    // piece 0: gate rows -> B rows 0..127; piece 1: up rows -> B rows 128..255
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma4<CM>(sb + q * (kBStage / 2), tB, bar, k0, j0, q, i);
   } else if constexpr (K == GemmKind::FC2) {
     const int i = kb / p.kb_per_shard;
     const int j0 = (kb - i * p.kb_per_shard) * kBK;
     tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
-    tma_load_3d(sb, tB, bar, j0, nt * kBN, i);
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma3<CM>(sb + q * (kBStage / 2), tB, bar, j0, nt * kBN + 128 * q, i);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
     tma_load_2d(sa, tA, bar, k0, mt * kBM);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
   } else if constexpr (K == GemmKind::DX) {
     tma_load_2d(sa, tA, bar, k0, mt * kBM);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
   } else if constexpr (K == GemmKind::WGRAD_W2) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
 #pragma unroll
     for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
   } else {  // WGRAD_W1
 #pragma unroll
     for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
   }
 }
 
@@ -307,7 +344,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
   }
 }
 
-template <GemmKind K>
+template <GemmKind K, int CM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
@@ -325,14 +362,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
   const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  constexpr uint16_t kPairMask = static_cast<uint16_t>((1u << CM) - 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = blockIdx.x / CM;
+  const int nclusters = gridDim.x / CM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CM);  // one commit from each CTA of the pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
@@ -351,10 +392,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (CM > 1) cluster_sync();  // the peer's barriers exist before any multicast
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtx wc{abort_flag, p.err, p.wait_ns};
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int num_pm = (p.num_m_tiles + CM - 1) / CM;  // M-tile pairs (the last may be half
+  const int num_super = num_pm * p.num_n_tiles;        // phantom: its loads read fill values)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -362,10 +405,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
-      bool skip_once = p.fault_inject != 0 && blockIdx.x == 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        int mt, nt;
-        tile_coords(tile, p, mt, nt);
+      bool skip_once = p.fault_inject != 0 && cid == 0 && rank == 0;
+      for (int st = cid; st < num_super; st += nclusters) {
+        int mp, nt;
+        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
+        const int mt = mp * CM + rank;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
@@ -377,8 +421,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, kStageBytes);
-            issue_stage<K>(&tmA, &tmB, sA0 + stage * kAStage, sB0 + stage * kBStage, fb, mt, nt,
-                           kb, p);
+            issue_stage<K, CM>(&tmA, &tmB, sA0 + stage * kAStage, sB0 + stage * kBStage, fb, mt,
+                               nt, kb, rank, p);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
@@ -400,7 +444,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      for (int st = cid; st < num_super; st += nclusters, ++it) {
         const int buf = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
         if (!wait_bounded(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
@@ -423,7 +467,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                                 : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(empty0 + 8 * stage);
+          if constexpr (CM > 1) umma_commit_mc(empty0 + 8 * stage, kPairMask);
+          else umma_commit(empty0 + 8 * stage);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -441,7 +486,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    for (int st = cid; st < num_super; st += nclusters, ++it) {
       const int buf = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       int ok = 1;
@@ -450,10 +495,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      int mt, nt;
-      tile_coords(tile, p, mt, nt);
+      int mp, nt;
+      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
-      epilogue_tile<K>(tacc, row, mt, nt, p);
+      epilogue_tile<K>(tacc, row, mp * CM + rank, nt, p);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
@@ -463,6 +508,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Neither CTA of a pair leaves while the other may still multicast into its shared
+  // memory or arrive on its barriers.
+  if constexpr (CM > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);

@@ -4,34 +4,67 @@
 
 namespace mlpb {
 
+template <GemmKind K>
+static cudaError_t set_attr() {
+  return cudaFuncSetAttribute(gemm_kernel<K, kClusterM>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+}
+
+// `clusters` clusters of kClusterM CTAs, one CTA per SM.
+template <GemmKind K>
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                              int clusters, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kClusterM), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<K, kClusterM>, a, b, p);
+}
+
 cudaError_t gemm_fwd_set_smem_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<GemmKind::FC1_GELU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_kernel<GemmKind::FC1_SWIGLU>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_kernel<GemmKind::FC2>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = set_attr<GemmKind::FC1_GELU>();
+  if (e == cudaSuccess) e = set_attr<GemmKind::FC1_SWIGLU>();
+  if (e == cudaSuccess) e = set_attr<GemmKind::FC2>();
   return e;
 }
 
 cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
-                            const GemmParams& p, int grid, cudaStream_t s) {
+                            const GemmParams& p, int clusters, cudaStream_t s) {
   switch (kind) {
     case GemmKind::FC1_GELU:
-      gemm_kernel<GemmKind::FC1_GELU><<<grid, kGemmThreads, kGemmSmem, s>>>(a, b, p);
-      break;
+      return launch_one<GemmKind::FC1_GELU>(a, b, p, clusters, s);
     case GemmKind::FC1_SWIGLU:
-      gemm_kernel<GemmKind::FC1_SWIGLU><<<grid, kGemmThreads, kGemmSmem, s>>>(a, b, p);
-      break;
+      return launch_one<GemmKind::FC1_SWIGLU>(a, b, p, clusters, s);
     case GemmKind::FC2:
-      gemm_kernel<GemmKind::FC2><<<grid, kGemmThreads, kGemmSmem, s>>>(a, b, p);
-      break;
+      return launch_one<GemmKind::FC2>(a, b, p, clusters, s);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+}
+
+// Clusters of kClusterM GEMM CTAs that can be resident at once on this device.
+cudaError_t gemm_max_active_clusters(int* out) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * kClusterM, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, gemm_kernel<GemmKind::FC1_GELU, kClusterM>, &cfg);
 }
 
 }  // namespace mlpb

@@ -28,6 +28,7 @@ constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x 64(K) MN-major box, 8 KB
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 + 256;
+constexpr int kClusterM = 2;  // CTAs per cluster sharing each B tile (multicast)
 
 struct GemmParams {
   int num_m_tiles, num_n_tiles, num_kb;

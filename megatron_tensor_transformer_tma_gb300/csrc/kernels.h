@@ -9,18 +9,25 @@
 
 namespace mlpb {
 
-// gemm_fwd.cu / gemm_bwd.cu: one persistent launch of the tcgen05 GEMM of `kind`.
+// gemm_fwd.cu / gemm_bwd.cu: one persistent launch of the tcgen05 GEMM of `kind` on
+// `clusters` clusters of kClusterM CTAs.
 cudaError_t gemm_fwd_set_smem_attrs();
 cudaError_t gemm_bwd_set_smem_attrs();
+cudaError_t gemm_max_active_clusters(int* out);
 cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
-                            const GemmParams& p, int grid, cudaStream_t s);
+                            const GemmParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
-                            const GemmParams& p, int grid, cudaStream_t s);
+                            const GemmParams& p, int clusters, cudaStream_t s);
 
 // reduce.cu: column sums of a [R][C] bf16 matrix into fp32, deterministic two passes.
 //   pass 1: part[split][C] over row splits of `rows_per_split` rows; pass 2: out[C].
 cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int64_t rows_per_split, float* part, float* out, cudaStream_t s);
+// The same column sums in one launch: `counters` holds ceil(C/512) zeroed words that the
+// kernel leaves zeroed again.
+cudaError_t launch_colsum_bf16_fused(const void* in, int64_t R, int64_t C, int splits,
+                                     int64_t rows_per_split, float* part, float* out,
+                                     unsigned int* counters, cudaStream_t s);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.

@@ -2,8 +2,10 @@
 //
 // Both kernels stream whole rows into a ring of shared-memory buffers with TMA bulk
 // copies (cp.async.bulk), so the next rows' loads stay in flight while the CTA reduces
-// and writes the current one.  256 threads per CTA; thread i owns the 16-byte vectors
-// i, i+256, ... of the row (kVpt vectors), so every global store is coalesced.
+// and writes the current one.  Thread i of a CTA owns the 16-byte vectors i, i+NT, ...
+// of the row (kVpt vectors), so every global store is coalesced.  The forward uses
+// small CTAs (128 threads, up to four per SM) and the backward 256-thread CTAs, two per
+// SM, so that several rows' reduction chains overlap on every SM.
 //
 // Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row the mean and
 // the biased variance are two passes over the register-resident row (warp shuffles, then
@@ -25,10 +27,11 @@
 
 namespace mlpb {
 
-constexpr int kLnThreads = 256;
+constexpr int kLnFwdThreads = 128;
+constexpr int kLnBwdThreads = 256;
 
-template <int NV>
-__device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [8*NV] */) {
+template <int NT, int NV>
+__device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [NT/32 * NV] */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int k = 0; k < NV; ++k)
@@ -43,7 +46,7 @@ __device__ __forceinline__ void block_sum(float (&v)[NV], float* sh /* [8*NV] */
   for (int k = 0; k < NV; ++k) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kLnThreads / 32; ++w) s += sh[w * NV + k];
+    for (int w = 0; w < NT / 32; ++w) s += sh[w * NV + k];
     v[k] = s;
   }
 }
@@ -75,13 +78,14 @@ __device__ __forceinline__ void st_f32x8(float* p, const float* o) {
 
 // ------------------------------------------------------------------ forward
 template <int kVpt>
-__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
+__global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ Xn,
     float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
+  constexpr int NT = kLnFwdThreads;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float sh[8];
+  __shared__ float sh[NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t buf0 = smem_u32(smem);
@@ -101,21 +105,6 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
   }
   __syncthreads();
 
-  float gm[kVpt][8], bt[kVpt][8];
-  bool ok_v[kVpt];
-#pragma unroll
-  for (int k = 0; k < kVpt; ++k) {
-    const int c = (threadIdx.x + k * kLnThreads) * 8;
-    ok_v[k] = c < H;
-    uint4 g = make_uint4(0, 0, 0, 0), b = g;
-    if (ok_v[k]) {
-      g = ld_global_nc_v4(gamma + c);
-      b = ld_global_nc_v4(beta + c);
-    }
-    bf16x8_to_f32(g, gm[k]);
-    bf16x8_to_f32(b, bt[k]);
-  }
-
   int64_t issued = nbuf < n_mine ? nbuf : n_mine;
   for (int64_t i = 0; i < n_mine; ++i) {
     const int b = static_cast<int>(i % nbuf);
@@ -127,13 +116,14 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
     float s[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
+      const int vi = threadIdx.x + k * NT;
       uint4 u = make_uint4(0, 0, 0, 0);
-      if (ok_v[k]) u = ld_shared_v4(buf0 + b * row_bytes + (threadIdx.x + k * kLnThreads) * 16);
+      if (vi * 8 < H) u = ld_shared_v4(buf0 + b * row_bytes + vi * 16);
       bf16x8_to_f32(u, v[k]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s[0] += v[k][e];
     }
-    block_sum<1>(s, sh);  // every thread has read buffer b once this returns
+    block_sum<NT, 1>(s, sh);  // every thread has read buffer b once this returns
     if (threadIdx.x == 0 && issued < n_mine) {
       const int64_t nrow = blockIdx.x + issued * gridDim.x;
       fence_proxy_async_smem();
@@ -145,21 +135,23 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
     float q[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < kVpt; ++k)
-      if (ok_v[k])
+      if ((threadIdx.x + k * NT) * 8 < H)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float d = v[k][e] - mu;
           q[0] += d * d;
         }
-    block_sum<1>(q, sh);
+    block_sum<NT, 1>(q, sh);
     const float r = rsqrtf(q[0] / static_cast<float>(H) + eps);
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
-      if (!ok_v[k]) continue;
-      const int c = (threadIdx.x + k * kLnThreads) * 8;
-      float o[8];
+      const int c = (threadIdx.x + k * NT) * 8;
+      if (c >= H) continue;
+      float gm[8], bt[8], o[8];
+      bf16x8_to_f32(ld_global_nc_v4(gamma + c), gm);
+      bf16x8_to_f32(ld_global_nc_v4(beta + c), bt);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mu) * r * gm[k][e] + bt[k][e];
+      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mu) * r * gm[e] + bt[e];
       st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
     }
@@ -178,14 +170,15 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(
 
 // ------------------------------------------------------------------ backward
 template <int kVpt>
-__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
+__global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
     const float* __restrict__ mean, const float* __restrict__ rstd,
     const float* __restrict__ dXn, float* __restrict__ dX, float* __restrict__ part_dg,
     float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
+  constexpr int NT = kLnBwdThreads;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float sh[16];
+  __shared__ float sh[2 * NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 6u;  // X bf16 then dXn fp32
@@ -212,18 +205,27 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
   }
   __syncthreads();
 
-  float gm[kVpt][8], adg[kVpt][8], adb[kVpt][8];
-  bool ok_v[kVpt];
+  uint4 gpk[kVpt];  // gamma, kept packed (bf16) to leave registers for the partials
+  float adg[kVpt][8], adb[kVpt][8];
 #pragma unroll
   for (int k = 0; k < kVpt; ++k) {
-    const int c = (threadIdx.x + k * kLnThreads) * 8;
-    ok_v[k] = c < H;
-    uint4 g = make_uint4(0, 0, 0, 0);
-    if (ok_v[k]) g = ld_global_nc_v4(gamma + c);
-    bf16x8_to_f32(g, gm[k]);
+    const int c = (threadIdx.x + k * NT) * 8;
+    gpk[k] = make_uint4(0, 0, 0, 0);
+    if (c < H) gpk[k] = ld_global_nc_v4(gamma + c);
 #pragma unroll
     for (int e = 0; e < 8; ++e) adg[k][e] = adb[k][e] = 0.f;
   }
+
+  // x and dy of vector vi of the row in buffer (xb, db)
+  auto load_vec = [&](uint32_t xb, uint32_t db, int vi, float* x, float* dy) {
+    bf16x8_to_f32(ld_shared_v4(xb + vi * 16), x);
+    const uint4 d0 = ld_shared_v4(db + vi * 32);
+    const uint4 d1 = ld_shared_v4(db + vi * 32 + 16);
+    dy[0] = __uint_as_float(d0.x); dy[1] = __uint_as_float(d0.y);
+    dy[2] = __uint_as_float(d0.z); dy[3] = __uint_as_float(d0.w);
+    dy[4] = __uint_as_float(d1.x); dy[5] = __uint_as_float(d1.y);
+    dy[6] = __uint_as_float(d1.z); dy[7] = __uint_as_float(d1.w);
+  };
 
   int64_t issued = nbuf < n_mine ? nbuf : n_mine;
   for (int64_t i = 0; i < n_mine; ++i) {
@@ -235,51 +237,49 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const float mu = mean[row], rs = rstd[row];
     const uint32_t xb = buf0 + b * row_bytes;
     const uint32_t db = xb + xbytes;
-    float xh[kVpt][8], dy[kVpt][8];
+    // pass 1: sum g and sum g*xhat
     float s[2] = {0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
-      const uint32_t vi = threadIdx.x + k * kLnThreads;
-      uint4 ux = make_uint4(0, 0, 0, 0), d0 = ux, d1 = ux;
-      if (ok_v[k]) {
-        ux = ld_shared_v4(xb + vi * 16);
-        d0 = ld_shared_v4(db + vi * 32);
-        d1 = ld_shared_v4(db + vi * 32 + 16);
-      }
-      bf16x8_to_f32(ux, xh[k]);
-      dy[k][0] = __uint_as_float(d0.x); dy[k][1] = __uint_as_float(d0.y);
-      dy[k][2] = __uint_as_float(d0.z); dy[k][3] = __uint_as_float(d0.w);
-      dy[k][4] = __uint_as_float(d1.x); dy[k][5] = __uint_as_float(d1.y);
-      dy[k][6] = __uint_as_float(d1.z); dy[k][7] = __uint_as_float(d1.w);
+      const int vi = threadIdx.x + k * NT;
+      if (vi * 8 >= H) continue;
+      float x[8], dy[8], gm[8];
+      load_vec(xb, db, vi, x, dy);
+      bf16x8_to_f32(gpk[k], gm);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        xh[k][e] = ok_v[k] ? (xh[k][e] - mu) * rs : 0.f;
-        const float g = dy[k][e] * gm[k][e];
+        const float xh = (x[e] - mu) * rs;
+        const float g = dy[e] * gm[e];
         s[0] += g;
-        s[1] += g * xh[k][e];
+        s[1] += g * xh;
       }
     }
-    block_sum<2>(s, sh);  // every thread has read buffer b once this returns
+    block_sum<NT, 2>(s, sh);
+    const float mg = s[0] / static_cast<float>(H);
+    const float mgx = s[1] / static_cast<float>(H);
+    // pass 2: dx, and this CTA's dgamma / dbeta partials
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k) {
+      const int vi = threadIdx.x + k * NT;
+      if (vi * 8 >= H) continue;
+      float x[8], dy[8], gm[8], o[8];
+      load_vec(xb, db, vi, x, dy);
+      bf16x8_to_f32(gpk[k], gm);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xh = (x[e] - mu) * rs;
+        o[e] = rs * (dy[e] * gm[e] - mg - xh * mgx);
+        adg[k][e] += dy[e] * xh;
+        adb[k][e] += dy[e];
+      }
+      st_f32x8(dX + row * H + vi * 8, o);
+    }
+    __syncthreads();  // every thread has read buffer b
     if (threadIdx.x == 0 && issued < n_mine) {
       fence_proxy_async_smem();
       issue(b, issued);
     }
     ++issued;
-    const float mg = s[0] / static_cast<float>(H);
-    const float mgx = s[1] / static_cast<float>(H);
-#pragma unroll
-    for (int k = 0; k < kVpt; ++k) {
-      if (!ok_v[k]) continue;
-      const int c = (threadIdx.x + k * kLnThreads) * 8;
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        o[e] = rs * (dy[k][e] * gm[k][e] - mg - xh[k][e] * mgx);
-        adg[k][e] += dy[k][e] * xh[k][e];
-        adb[k][e] += dy[k][e];
-      }
-      st_f32x8(dX + row * H + c, o);
-    }
   }
   if (threadIdx.x == 0 && abort_flag) {
     const int64_t first = issued - nbuf > 0 ? issued - nbuf : 0;
@@ -288,17 +288,17 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
   }
 #pragma unroll
   for (int k = 0; k < kVpt; ++k) {
-    if (!ok_v[k]) continue;
-    const int c = (threadIdx.x + k * kLnThreads) * 8;
+    const int c = (threadIdx.x + k * NT) * 8;
+    if (c >= H) continue;
     st_f32x8(part_dg + static_cast<int64_t>(blockIdx.x) * H + c, adg[k]);
     st_f32x8(part_db + static_cast<int64_t>(blockIdx.x) * H + c, adb[k]);
   }
 }
 
 // ------------------------------------------------------------------ launchers
-static int ln_vpt(int64_t H) {
-  const int64_t v = (H / 8 + kLnThreads - 1) / kLnThreads;
-  return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : 8;
+static int ln_vpt(int64_t H, int threads) {
+  const int64_t v = (H / 8 + threads - 1) / threads;
+  return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : v <= 8 ? 8 : 16;
 }
 
 template <class K>
@@ -312,27 +312,28 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
                           uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const size_t row = static_cast<size_t>(H) * 2;
-  int nbuf = static_cast<int>(std::min<size_t>(4, std::max<size_t>(2, (96u << 10) / row)));
+  const int nbuf = static_cast<int>(std::min<size_t>(3, std::max<size_t>(2, (48u << 10) / row)));
   const size_t smem = nbuf * row + 8 * nbuf;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(T, 2 * num_sms));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(T, 4 * num_sms));
   const auto* x = static_cast<const __nv_bfloat16*>(X);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
   auto* xn = static_cast<__nv_bfloat16*>(Xn);
   const int Hi = static_cast<int>(H);
   cudaError_t e = cudaSuccess;
-  switch (ln_vpt(H)) {
-#define MLPB_LN_FWD(V)                                                                     \
-  case V:                                                                                  \
-    e = set_smem(ln_fwd_kernel<V>, smem);                                                  \
-    if (e == cudaSuccess)                                                                  \
-      ln_fwd_kernel<V><<<grid, kLnThreads, smem, s>>>(x, g, b, xn, mean, rstd, T, Hi, eps, \
-                                                      nbuf, err, wait_ns);                 \
+  switch (ln_vpt(H, kLnFwdThreads)) {
+#define MLPB_LN_FWD(V)                                                                        \
+  case V:                                                                                     \
+    e = set_smem(ln_fwd_kernel<V>, smem);                                                     \
+    if (e == cudaSuccess)                                                                     \
+      ln_fwd_kernel<V><<<grid, kLnFwdThreads, smem, s>>>(x, g, b, xn, mean, rstd, T, Hi, eps, \
+                                                         nbuf, err, wait_ns);                 \
     break;
     MLPB_LN_FWD(1)
     MLPB_LN_FWD(2)
     MLPB_LN_FWD(4)
     MLPB_LN_FWD(8)
+    MLPB_LN_FWD(16)
 #undef MLPB_LN_FWD
   }
   if (e != cudaSuccess) return e;
@@ -344,7 +345,7 @@ cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, c
                           int64_t T, int64_t H, int shards, int blocks_per_shard, uint32_t* err,
                           uint64_t wait_ns, cudaStream_t s) {
   const size_t row = static_cast<size_t>(H) * 6;
-  int nbuf = static_cast<int>(std::min<size_t>(4, std::max<size_t>(2, (160u << 10) / row)));
+  const int nbuf = 2;  // two 256-thread CTAs per SM, each with a two-row ring
   const size_t smem = nbuf * row + 8 * nbuf;
   const unsigned grid = static_cast<unsigned>(shards * blocks_per_shard);
   const auto* x = static_cast<const __nv_bfloat16*>(X);
@@ -352,14 +353,14 @@ cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, c
   const int Hi = static_cast<int>(H);
   const int64_t rps = T / shards;
   cudaError_t e = cudaSuccess;
-  switch (ln_vpt(H)) {
-#define MLPB_LN_BWD(V)                                                                       \
-  case V:                                                                                    \
-    e = set_smem(ln_bwd_kernel<V>, smem);                                                    \
-    if (e == cudaSuccess)                                                                    \
-      ln_bwd_kernel<V><<<grid, kLnThreads, smem, s>>>(x, g, mean, rstd, dXn, dX, part_dg,    \
-                                                      part_db, rps, blocks_per_shard, Hi,    \
-                                                      nbuf, err, wait_ns);                   \
+  switch (ln_vpt(H, kLnBwdThreads)) {
+#define MLPB_LN_BWD(V)                                                                          \
+  case V:                                                                                       \
+    e = set_smem(ln_bwd_kernel<V>, smem);                                                       \
+    if (e == cudaSuccess)                                                                       \
+      ln_bwd_kernel<V><<<grid, kLnBwdThreads, smem, s>>>(x, g, mean, rstd, dXn, dX, part_dg,    \
+                                                         part_db, rps, blocks_per_shard, Hi,    \
+                                                         nbuf, err, wait_ns);                   \
     break;
     MLPB_LN_BWD(1)
     MLPB_LN_BWD(2)

@@ -58,6 +58,73 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
+// One-launch variant: pass 1 as above, then the last CTA to finish a 512-column chunk
+// (found with a per-chunk arrival counter) sums that chunk's partials in split order and
+// re-arms the counter to zero.  The order of the final sum never depends on timing.
+__global__ void __launch_bounds__(256) colsum_bf16_fused_kernel(
+    const __nv_bfloat16* __restrict__ in, int64_t R, int64_t C, int64_t rows_per_split,
+    float* part, float* __restrict__ out, unsigned int* counters) {
+  __shared__ float red[kRowLanes - 1][64][9];
+  __shared__ unsigned int last;
+  const int cv = threadIdx.x & 63;
+  const int rl = threadIdx.x >> 6;
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * kColsPerCta + cv * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_split;
+  const int64_t r1 = min(R, r0 + rows_per_split);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (col < C) {
+    const __nv_bfloat16* p = in + col;
+    int64_t r = r0 + rl;
+#pragma unroll 8
+    for (; r < r1; r += kRowLanes) {
+      const uint4 u = ld_global_nc_v4(p + r * C);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
+    }
+  }
+  if (rl > 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[rl - 1][cv][e] = acc[e];
+  }
+  __syncthreads();
+  if (rl == 0 && col < C) {
+#pragma unroll
+    for (int l = 0; l < kRowLanes - 1; ++l)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += red[l][cv][e];
+    float* o = part + static_cast<int64_t>(blockIdx.y) * C + col;
+    st_global_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                               __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+    st_global_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                   __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+  }
+  __threadfence();  // partials visible device-wide before the arrival is counted
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int prev = atomicAdd(&counters[blockIdx.x], 1u);
+    last = (prev == gridDim.y - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // the last CTA of this chunk: 512 columns, 256 threads x 2 columns, splits in order
+  for (int j = threadIdx.x; j < kColsPerCta; j += blockDim.x) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * kColsPerCta + j;
+    if (c >= C) break;
+    float t = 0.f;
+    for (unsigned int k = 0; k < gridDim.y; ++k) t += __ldcg(part + static_cast<int64_t>(k) * C + c);
+    out[c] = t;
+  }
+  if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
+}
+
 // out[c] = sum_k part[k][c] for one or two partial arrays (blockIdx.y picks the array).
 // A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
 // eight warp sums are added in warp order -- a fixed order, so results are reproducible.
@@ -101,6 +168,16 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_sum_partials(part, splits, C, out, s);
+}
+
+cudaError_t launch_colsum_bf16_fused(const void* in, int64_t R, int64_t C, int splits,
+                                     int64_t rows_per_split, float* part, float* out,
+                                     unsigned int* counters, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((C + kColsPerCta - 1) / kColsPerCta),
+                  static_cast<unsigned>(splits));
+  colsum_bf16_fused_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), R, C,
+                                                 rows_per_split, part, out, counters);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
