@@ -77,12 +77,10 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// Read-only 16-byte load (ld.global.nc).  Not an asm volatile: the compiler must be free
+// to hoist a batch of these ahead of their uses so that they are in flight together.
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+  return __ldg(static_cast<const uint4*>(p));
 }
 
 }  // namespace mlpb

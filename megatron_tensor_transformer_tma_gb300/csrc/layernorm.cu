@@ -61,12 +61,14 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
+// Dynamic shared memory of the LN kernels (rows, then the ring's mbarriers).
+extern __shared__ __align__(128) uint8_t ln_smem[];
+
+// 16-byte load from the ring at byte offset `off` of the dynamic shared memory.  A plain
+// load, so batches of them can be issued together; the mbarrier wait before them is an
+// asm volatile with a memory clobber, which they cannot be moved above.
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t off) {
+  return *reinterpret_cast<const uint4*>(ln_smem + off);
 }
 
 __device__ __forceinline__ void st_f32x8(float* p, const float* o) {
@@ -84,11 +86,10 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnFwdThreads;
-  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float sh[NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
-  const uint32_t buf0 = smem_u32(smem);
+  const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int64_t n_mine = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
   const WaitCtx wc{&abort_flag, err, wait_ns};
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     for (int k = 0; k < kVpt; ++k) {
       const int vi = threadIdx.x + k * NT;
       uint4 u = make_uint4(0, 0, 0, 0);
-      if (vi * 8 < H) u = ld_shared_v4(buf0 + b * row_bytes + vi * 16);
+      if (vi * 8 < H) u = ld_shared_v4(b * row_bytes + vi * 16);
       bf16x8_to_f32(u, v[k]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s[0] += v[k][e];
@@ -177,12 +178,11 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnBwdThreads;
-  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float sh[2 * NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 6u;  // X bf16 then dXn fp32
-  const uint32_t buf0 = smem_u32(smem);
+  const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int shard = blockIdx.x / blocks_per_shard;
   const int bidx = blockIdx.x - shard * blocks_per_shard;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     if (!__syncthreads_and(ok)) break;
     const int64_t row = rbeg + bidx + i * blocks_per_shard;
     const float mu = mean[row], rs = rstd[row];
-    const uint32_t xb = buf0 + b * row_bytes;
+    const uint32_t xb = b * row_bytes;  // offsets into ln_smem
     const uint32_t db = xb + xbytes;
     // pass 1: sum g and sum g*xhat
     float s[2] = {0.f, 0.f};

@@ -11,6 +11,32 @@ namespace mlpb {
 
 constexpr int kColsPerCta = 512;
 constexpr int kRowLanes = 4;
+constexpr int kBatch = 8;  // 16-byte loads in flight per thread
+
+// acc[0..8) += column sums of 8 bf16 columns at p over rows r, r+4, ... < r1.  Loads are
+// issued in explicit batches of kBatch before any is consumed.
+__device__ __forceinline__ void add_bf16x8(const uint4& u, float (&acc)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = unpack_bf16x2(w[e]);
+    acc[2 * e] += f.x;
+    acc[2 * e + 1] += f.y;
+  }
+}
+
+__device__ __forceinline__ void colsum_rows(const __nv_bfloat16* p, int64_t C, int64_t r,
+                                            int64_t r1, float (&acc)[8]) {
+  // full batches: kBatch unconditional loads, then their sums
+  for (; r + (kBatch - 1) * kRowLanes < r1; r += kBatch * kRowLanes) {
+    uint4 u[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) u[j] = ld_global_nc_v4(p + (r + j * kRowLanes) * C);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) add_bf16x8(u[j], acc);
+  }
+  for (; r < r1; r += kRowLanes) add_bf16x8(ld_global_nc_v4(p + r * C), acc);
+}
 
 __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* __restrict__ in,
                                                           int64_t R, int64_t C,
@@ -26,19 +52,7 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   if (col < C) {
-    const __nv_bfloat16* p = in + col;
-    int64_t r = r0 + rl;
-#pragma unroll 8
-    for (; r < r1; r += kRowLanes) {
-      const uint4 u = ld_global_nc_v4(p + r * C);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(w[e]);
-        acc[2 * e] += f.x;
-        acc[2 * e + 1] += f.y;
-      }
-    }
+    colsum_rows(in + col, C, r0 + rl, r1, acc);
   }
   if (rl > 0) {
 #pragma unroll
@@ -75,19 +89,7 @@ __global__ void __launch_bounds__(256) colsum_bf16_fused_kernel(
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   if (col < C) {
-    const __nv_bfloat16* p = in + col;
-    int64_t r = r0 + rl;
-#pragma unroll 8
-    for (; r < r1; r += kRowLanes) {
-      const uint4 u = ld_global_nc_v4(p + r * C);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(w[e]);
-        acc[2 * e] += f.x;
-        acc[2 * e + 1] += f.y;
-      }
-    }
+    colsum_rows(in + col, C, r0 + rl, r1, acc);
   }
   if (rl > 0) {
 #pragma unroll
