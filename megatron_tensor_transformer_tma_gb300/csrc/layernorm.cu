@@ -3,13 +3,12 @@
 // Both kernels stream whole rows into a ring of shared-memory buffers with TMA bulk
 // copies (cp.async.bulk), so the next rows' loads stay in flight while the CTA reduces
 // and writes the current one.  Thread i of a CTA owns the 16-byte vectors i, i+NT, ...
-// of the row (kVpt vectors), so every global store is coalesced.  The forward uses
-// small CTAs (128 threads, up to four per SM) and the backward 256-thread CTAs, two per
-// SM, so that several rows' reduction chains overlap on every SM.
+// of the row (kVpt vectors), so every global store is coalesced.  256-thread CTAs, two
+// or more per SM, so that several rows' reduction chains overlap on every SM.
 //
-// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row the mean and
-// the biased variance are two passes over the register-resident row (warp shuffles, then
-// one value per warp through shared memory); Xn = (x - mu) rstd gamma + beta in bf16.
+// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row each thread
+// takes the exact mean and sum of squared deviations of its register-resident values and
+// one block reduction merges them (biased variance); Xn = (x - mu) rstd gamma + beta.
 // Sequence shard s owns rows [s T/t, (s+1) T/t); rows are independent, so the forward
 // needs no shard structure and the emulated all-gather is the row layout of Xn itself.
 //
@@ -27,7 +26,7 @@
 
 namespace mlpb {
 
-constexpr int kLnFwdThreads = 128;
+constexpr int kLnFwdThreads = 256;
 constexpr int kLnBwdThreads = 256;
 
 template <int NT, int NV>
@@ -79,6 +78,21 @@ __device__ __forceinline__ void st_f32x8(float* p, const float* o) {
 }
 
 // ------------------------------------------------------------------ forward
+// Per thread: exact mean and M2 = sum (x - mean)^2 of its own register-resident values;
+// per CTA: one reduction merging the (count, mean, M2) triples of the threads in a fixed
+// order (Chan et al.'s pairwise update), so each row needs a single block reduction.
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& m2, float nb, float mb,
+                                           float m2b) {
+  const float nn = n + nb;
+  if (nn > 0.f) {
+    const float d = mb - m;
+    const float f = nb / nn;
+    m += d * f;
+    m2 += m2b + d * d * n * f;
+    n = nn;
+  }
+}
+
 template <int kVpt>
 __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
@@ -86,13 +100,15 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnFwdThreads;
-  __shared__ float sh[NT / 32];
+  constexpr int NW = NT / 32;
+  __shared__ float shn[NW], shm[NW], shq[NW];
   __shared__ uint32_t abort_flag;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int64_t n_mine = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
   const WaitCtx wc{&abort_flag, err, wait_ns};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
     abort_flag = 0u;
@@ -102,6 +118,19 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       const int64_t row = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
       mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
       bulk_load(buf0 + b * row_bytes, X + row * H, row_bytes, bar0 + 8 * b);
+    }
+  }
+  // gamma and beta stay packed (bf16) in registers for the whole kernel
+  uint4 gpk[kVpt], bpk[kVpt];
+  int nvalid = 0;
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int c = (threadIdx.x + k * NT) * 8;
+    gpk[k] = bpk[k] = make_uint4(0, 0, 0, 0);
+    if (c < H) {
+      gpk[k] = ld_global_nc_v4(gamma + c);
+      bpk[k] = ld_global_nc_v4(beta + c);
+      nvalid += 8;
     }
   }
   __syncthreads();
@@ -114,7 +143,7 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     if (!__syncthreads_and(ok)) break;
     const int64_t row = blockIdx.x + i * gridDim.x;
     float v[kVpt][8];
-    float s[1] = {0.f};
+    float sum = 0.f;
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int vi = threadIdx.x + k * NT;
@@ -122,9 +151,34 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       if (vi * 8 < H) u = ld_shared_v4(b * row_bytes + vi * 16);
       bf16x8_to_f32(u, v[k]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s[0] += v[k][e];
+      for (int e = 0; e < 8; ++e) sum += v[k][e];
     }
-    block_sum<NT, 1>(s, sh);  // every thread has read buffer b once this returns
+    // this thread's exact (count, mean, M2)
+    float n = static_cast<float>(nvalid);
+    float m = nvalid ? sum / n : 0.f;
+    float m2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k)
+      if ((threadIdx.x + k * NT) * 8 < H)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = v[k][e] - m;
+          m2 += d * d;
+        }
+    // merge across the warp, then across warps in warp order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+      const float mb = __shfl_xor_sync(0xffffffffu, m, o);
+      const float qb = __shfl_xor_sync(0xffffffffu, m2, o);
+      chan_merge(n, m, m2, nb, mb, qb);
+    }
+    if (lane == 0) {
+      shn[warp] = n;
+      shm[warp] = m;
+      shq[warp] = m2;
+    }
+    __syncthreads();  // also: every thread has read buffer b
     if (threadIdx.x == 0 && issued < n_mine) {
       const int64_t nrow = blockIdx.x + issued * gridDim.x;
       fence_proxy_async_smem();
@@ -132,27 +186,22 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       bulk_load(buf0 + b * row_bytes, X + nrow * H, row_bytes, bar0 + 8 * b);
     }
     ++issued;
-    const float mu = s[0] / static_cast<float>(H);
-    float q[1] = {0.f};
+    float N = shn[0], mu = shm[0], M2 = shq[0];
 #pragma unroll
-    for (int k = 0; k < kVpt; ++k)
-      if ((threadIdx.x + k * NT) * 8 < H)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = v[k][e] - mu;
-          q[0] += d * d;
-        }
-    block_sum<NT, 1>(q, sh);
-    const float r = rsqrtf(q[0] / static_cast<float>(H) + eps);
+    for (int w = 1; w < NW; ++w) chan_merge(N, mu, M2, shn[w], shm[w], shq[w]);
+    const float r = rsqrtf(M2 / static_cast<float>(H) + eps);
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int c = (threadIdx.x + k * NT) * 8;
       if (c >= H) continue;
       float gm[8], bt[8], o[8];
-      bf16x8_to_f32(ld_global_nc_v4(gamma + c), gm);
-      bf16x8_to_f32(ld_global_nc_v4(beta + c), bt);
+      bf16x8_to_f32(gpk[k], gm);
+      bf16x8_to_f32(bpk[k], bt);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mu) * r * gm[e] + bt[e];
+      for (int e = 0; e < 8; ++e) {
+        const float a = r * gm[e];
+        o[e] = fmaf(v[k][e] - mu, a, bt[e]);
+      }
       st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
     }
@@ -160,6 +209,7 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       mean[row] = mu;
       rstd[row] = r;
     }
+    __syncthreads();  // shn/shm/shq are rewritten by the next row
   }
   // Copies still in flight (only after an abort) must land before the CTA exits.
   if (threadIdx.x == 0 && abort_flag) {
@@ -314,7 +364,6 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
   const size_t row = static_cast<size_t>(H) * 2;
   const int nbuf = static_cast<int>(std::min<size_t>(3, std::max<size_t>(2, (48u << 10) / row)));
   const size_t smem = nbuf * row + 8 * nbuf;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(T, 4 * num_sms));
   const auto* x = static_cast<const __nv_bfloat16*>(X);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
@@ -323,12 +372,19 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
   cudaError_t e = cudaSuccess;
   switch (ln_vpt(H, kLnFwdThreads)) {
 #define MLPB_LN_FWD(V)                                                                        \
-  case V:                                                                                     \
+  case V: {                                                                                   \
     e = set_smem(ln_fwd_kernel<V>, smem);                                                     \
+    int per_sm = 1;                                                                           \
+    if (e == cudaSuccess)                                                                     \
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_fwd_kernel<V>,            \
+                                                        kLnFwdThreads, smem);                 \
+    const unsigned grid =                                                                     \
+        static_cast<unsigned>(std::min<int64_t>(T, std::max(1, per_sm) * num_sms));           \
     if (e == cudaSuccess)                                                                     \
       ln_fwd_kernel<V><<<grid, kLnFwdThreads, smem, s>>>(x, g, b, xn, mean, rstd, T, Hi, eps, \
                                                          nbuf, err, wait_ns);                 \
-    break;
+    break;                                                                                    \
+  }
     MLPB_LN_FWD(1)
     MLPB_LN_FWD(2)
     MLPB_LN_FWD(4)

@@ -116,13 +116,53 @@ __global__ void __launch_bounds__(256) colsum_bf16_fused_kernel(
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // the last CTA of this chunk: 512 columns, 256 threads x 2 columns, splits in order
-  for (int j = threadIdx.x; j < kColsPerCta; j += blockDim.x) {
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * kColsPerCta + j;
-    if (c >= C) break;
-    float t = 0.f;
-    for (unsigned int k = 0; k < gridDim.y; ++k) t += __ldcg(part + static_cast<int64_t>(k) * C + c);
-    out[c] = t;
+  // The last CTA of this chunk: thread (cv, rl) sums splits rl, rl+4, ... of its 8
+  // columns, four splits' loads in flight at a time; the four row lanes are then added
+  // in lane order.
+  float t[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) t[e] = 0.f;
+  if (col < C) {
+    const int ns = static_cast<int>(gridDim.y);
+    int k = rl;
+    for (; k + 3 * kRowLanes < ns; k += 4 * kRowLanes) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float* q = part + static_cast<int64_t>(k + j * kRowLanes) * C + col;
+        v[2 * j] = __ldcg(reinterpret_cast<const float4*>(q));
+        v[2 * j + 1] = __ldcg(reinterpret_cast<const float4*>(q + 4));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        t[0] += v[2 * j].x; t[1] += v[2 * j].y; t[2] += v[2 * j].z; t[3] += v[2 * j].w;
+        t[4] += v[2 * j + 1].x; t[5] += v[2 * j + 1].y; t[6] += v[2 * j + 1].z;
+        t[7] += v[2 * j + 1].w;
+      }
+    }
+    for (; k < ns; k += kRowLanes) {
+      const float* q = part + static_cast<int64_t>(k) * C + col;
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(q));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(q + 4));
+      t[0] += a.x; t[1] += a.y; t[2] += a.z; t[3] += a.w;
+      t[4] += b.x; t[5] += b.y; t[6] += b.z; t[7] += b.w;
+    }
+  }
+  __syncthreads();  // red[] is reused
+  if (rl > 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[rl - 1][cv][e] = t[e];
+  }
+  __syncthreads();
+  if (rl == 0 && col < C) {
+#pragma unroll
+    for (int l = 0; l < kRowLanes - 1; ++l)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t[e] += red[l][cv][e];
+    st_global_v4(out + col, make_uint4(__float_as_uint(t[0]), __float_as_uint(t[1]),
+                                       __float_as_uint(t[2]), __float_as_uint(t[3])));
+    st_global_v4(out + col + 4, make_uint4(__float_as_uint(t[4]), __float_as_uint(t[5]),
+                                           __float_as_uint(t[6]), __float_as_uint(t[7])));
   }
   if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
 }
