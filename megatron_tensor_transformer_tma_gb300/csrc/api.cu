@@ -83,8 +83,7 @@ struct mlpb_handle {
   int device;
   int num_sms;
   int max_clusters;  // co-resident GEMM clusters
-  uint32_t* d_err;            // [0]: device error word; [64..]: colsum chunk counters
-  unsigned int* d_counters;
+  uint32_t* d_err;  // device error word
   bool fault_pending;
   uint64_t wait_ns;
   // bias-grad split plans
@@ -160,12 +159,6 @@ mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap&
                       : launch_gemm_bwd(kind, a, b, p, clusters, s);
   lt.done();
   return from_cuda(e);
-}
-
-// Error word plus one zeroed arrival counter per 512-column chunk of the widest column
-// sum (db1 over F or db2 over H).
-size_t kDevWordsBytes(const mlpb_handle* h) {
-  return (64 + static_cast<size_t>(cdiv(std::max(h->F, h->H), 512))) * sizeof(uint32_t);
 }
 
 size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
@@ -259,13 +252,12 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   }
   if (load_encoder() != MLPB_OK || gemm_fwd_set_smem_attrs() != cudaSuccess ||
       gemm_bwd_set_smem_attrs() != cudaSuccess ||
-      cudaMalloc(reinterpret_cast<void**>(&h->d_err), kDevWordsBytes(h)) != cudaSuccess ||
-      cudaMemset(h->d_err, 0, kDevWordsBytes(h)) != cudaSuccess) {
+      cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
     if (h->d_err) cudaFree(h->d_err);
     delete h;
     return MLPB_ECUDA;
   }
-  h->d_counters = reinterpret_cast<unsigned int*>(h->d_err + 64);
   if (gemm_max_active_clusters(&h->max_clusters) != cudaSuccess || h->max_clusters < 1) {
     cudaFree(h->d_err);
     delete h;
@@ -414,9 +406,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 1);
-    cudaError_t e = launch_colsum_bf16_fused(dY, T, H, h->db2_splits, h->db2_rows, part2, db2,
-                                             h->d_counters, s);
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
+    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
   }
@@ -446,9 +437,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- db1 = sum_t dZ
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 1);
-    cudaError_t e = launch_colsum_bf16_fused(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1,
-                                             h->d_counters, s);
+    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
+    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s);
     lt.done();
     if ((st = from_cuda(e)) != MLPB_OK) return st;
   }

@@ -23,11 +23,6 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
 //   pass 1: part[split][C] over row splits of `rows_per_split` rows; pass 2: out[C].
 cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int64_t rows_per_split, float* part, float* out, cudaStream_t s);
-// The same column sums in one launch: `counters` holds ceil(C/512) zeroed words that the
-// kernel leaves zeroed again.
-cudaError_t launch_colsum_bf16_fused(const void* in, int64_t R, int64_t C, int splits,
-                                     int64_t rows_per_split, float* part, float* out,
-                                     unsigned int* counters, cudaStream_t s);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.

@@ -72,101 +72,6 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
-// One-launch variant: pass 1 as above, then the last CTA to finish a 512-column chunk
-// (found with a per-chunk arrival counter) sums that chunk's partials in split order and
-// re-arms the counter to zero.  The order of the final sum never depends on timing.
-__global__ void __launch_bounds__(256) colsum_bf16_fused_kernel(
-    const __nv_bfloat16* __restrict__ in, int64_t R, int64_t C, int64_t rows_per_split,
-    float* part, float* __restrict__ out, unsigned int* counters) {
-  __shared__ float red[kRowLanes - 1][64][9];
-  __shared__ unsigned int last;
-  const int cv = threadIdx.x & 63;
-  const int rl = threadIdx.x >> 6;
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * kColsPerCta + cv * 8;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_split;
-  const int64_t r1 = min(R, r0 + rows_per_split);
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  if (col < C) {
-    colsum_rows(in + col, C, r0 + rl, r1, acc);
-  }
-  if (rl > 0) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) red[rl - 1][cv][e] = acc[e];
-  }
-  __syncthreads();
-  if (rl == 0 && col < C) {
-#pragma unroll
-    for (int l = 0; l < kRowLanes - 1; ++l)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += red[l][cv][e];
-    float* o = part + static_cast<int64_t>(blockIdx.y) * C + col;
-    st_global_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                               __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-    st_global_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                                   __float_as_uint(acc[6]), __float_as_uint(acc[7])));
-  }
-  __threadfence();  // partials visible device-wide before the arrival is counted
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned int prev = atomicAdd(&counters[blockIdx.x], 1u);
-    last = (prev == gridDim.y - 1) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // The last CTA of this chunk: thread (cv, rl) sums splits rl, rl+4, ... of its 8
-  // columns, four splits' loads in flight at a time; the four row lanes are then added
-  // in lane order.
-  float t[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) t[e] = 0.f;
-  if (col < C) {
-    const int ns = static_cast<int>(gridDim.y);
-    int k = rl;
-    for (; k + 3 * kRowLanes < ns; k += 4 * kRowLanes) {
-      float4 v[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float* q = part + static_cast<int64_t>(k + j * kRowLanes) * C + col;
-        v[2 * j] = __ldcg(reinterpret_cast<const float4*>(q));
-        v[2 * j + 1] = __ldcg(reinterpret_cast<const float4*>(q + 4));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        t[0] += v[2 * j].x; t[1] += v[2 * j].y; t[2] += v[2 * j].z; t[3] += v[2 * j].w;
-        t[4] += v[2 * j + 1].x; t[5] += v[2 * j + 1].y; t[6] += v[2 * j + 1].z;
-        t[7] += v[2 * j + 1].w;
-      }
-    }
-    for (; k < ns; k += kRowLanes) {
-      const float* q = part + static_cast<int64_t>(k) * C + col;
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(q));
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(q + 4));
-      t[0] += a.x; t[1] += a.y; t[2] += a.z; t[3] += a.w;
-      t[4] += b.x; t[5] += b.y; t[6] += b.z; t[7] += b.w;
-    }
-  }
-  __syncthreads();  // red[] is reused
-  if (rl > 0) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) red[rl - 1][cv][e] = t[e];
-  }
-  __syncthreads();
-  if (rl == 0 && col < C) {
-#pragma unroll
-    for (int l = 0; l < kRowLanes - 1; ++l)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) t[e] += red[l][cv][e];
-    st_global_v4(out + col, make_uint4(__float_as_uint(t[0]), __float_as_uint(t[1]),
-                                       __float_as_uint(t[2]), __float_as_uint(t[3])));
-    st_global_v4(out + col + 4, make_uint4(__float_as_uint(t[4]), __float_as_uint(t[5]),
-                                           __float_as_uint(t[6]), __float_as_uint(t[7])));
-  }
-  if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
-}
-
 // out[c] = sum_k part[k][c] for one or two partial arrays (blockIdx.y picks the array).
 // A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
 // eight warp sums are added in warp order -- a fixed order, so results are reproducible.
@@ -210,16 +115,6 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_sum_partials(part, splits, C, out, s);
-}
-
-cudaError_t launch_colsum_bf16_fused(const void* in, int64_t R, int64_t C, int splits,
-                                     int64_t rows_per_split, float* part, float* out,
-                                     unsigned int* counters, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((C + kColsPerCta - 1) / kColsPerCta),
-                  static_cast<unsigned>(splits));
-  colsum_bf16_fused_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), R, C,
-                                                 rows_per_split, part, out, counters);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
