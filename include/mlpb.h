@@ -45,7 +45,11 @@
  *     nothing.  Outputs are overwritten, never accumulated into.
  *   - A device-side bounded wait that expires (about one second) is recorded in
  *     a per-handle error word and reported by mlpb_last_device_error().
- *   - A handle may be used from one host thread at a time.
+ *   - A handle may be used from one host thread at a time, and its calls must not
+ *     overlap on the GPU (issue them on one stream, or order the streams).
+ *     mlpb_backward runs part of its work on a second stream that the handle owns,
+ *     forked from and joined back into `stream` with events, so all of its work is
+ *     ordered before later work on `stream`.
  */
 #ifndef MLPB_H_
 #define MLPB_H_

@@ -90,6 +90,10 @@ struct mlpb_handle {
   int db2_splits, db1_splits;
   int64_t db2_rows, db1_rows;
   int ln_blocks_per_shard;
+  // second stream of the backward: the weight gradients and bias sums that do not
+  // depend on each other run beside the dgrad / dX GEMMs and fill their tails
+  cudaStream_t side;
+  cudaEvent_t ev_fork, ev_dz, ev_join;
   // timing
   bool timing;
   std::vector<TimedLaunch> launches;
@@ -263,6 +267,15 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
     delete h;
     return MLPB_ECUDA;
   }
+  h->side = nullptr;
+  h->ev_fork = h->ev_dz = h->ev_join = nullptr;
+  if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_dz, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    mlpb_destroy(h);
+    return MLPB_ECUDA;
+  }
   plan_colsum(h->T, h->H, h->num_sms, &h->db2_splits, &h->db2_rows);
   plan_colsum(h->T, h->F, h->num_sms, &h->db1_splits, &h->db1_rows);
   // LN backward: two CTAs per SM, split evenly over the t sequence shards
@@ -280,6 +293,10 @@ void mlpb_destroy(mlpb_handle* h) {
     cudaEventDestroy(l.stop);
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_dz) cudaEventDestroy(h->ev_dz);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
 }
@@ -403,18 +420,44 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
   float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
                                           align256(static_cast<size_t>(h->db2_splits) * H * 4));
+  cudaStream_t s2 = h->side;
 
-  // ---- db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
+  // Fork: stream s2 starts with everything that needs only dY and A.
+  if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(s2, h->ev_fork, 0) != cudaSuccess)
+    return MLPB_ECUDA;
+  CUtensorMap ta, tb;
+
+  // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
-    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s);
+    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
+    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s2);
     lt.done();
-    if ((st = from_cuda(e)) != MLPB_OK) return st;
+    st = from_cuda(e);
   }
 
-  CUtensorMap ta, tb;
-  // ---- dgrad of fc2 with the fused activation derivative: dZ [T][F1]
-  {
+  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
+  if (st == MLPB_OK) {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(H);
+    p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_kb = static_cast<int>(T / kBK);
+    p.out0 = dW2;
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
+                               static_cast<uint64_t>(t)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
+    const uint32_t bbox[3] = {64, kBK, 1};
+    if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
+      st = MLPB_EINVAL;
+    else
+      st = run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
+                    2.0 * (T * H + T * F) + 4.0 * H * F);
+  }
+
+  // ---- [s] dgrad of fc2 with the fused activation derivative: dZ [T][F1]
+  if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(T);
     p.num_m_tiles = static_cast<int>(T / kBM);
@@ -428,43 +471,26 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
     const uint32_t bbox[3] = {64, kBK, 1};
     if (!map2d(&ta, dY, H, T, H, kBK, kBM) || !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
-      return MLPB_EINVAL;
-    const double bytes = 2.0 * (T * H + F * H + 2 * T * F1);
-    st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, ta, tb, p,
-                  s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H, bytes);
-    if (st != MLPB_OK) return st;
+      st = MLPB_EINVAL;
+    else
+      st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, ta, tb,
+                    p, s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H,
+                    2.0 * (T * H + F * H + 2 * T * F1));
   }
+  if (st == MLPB_OK && (cudaEventRecord(h->ev_dz, s) != cudaSuccess ||
+                        cudaStreamWaitEvent(s2, h->ev_dz, 0) != cudaSuccess))
+    st = MLPB_ECUDA;
 
-  // ---- db1 = sum_t dZ
-  if (bias) {
-    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
-    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s);
+  // ---- [s2] db1 = sum_t dZ
+  if (st == MLPB_OK && bias) {
+    LaunchTimer lt(h, s2, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
+    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s2);
     lt.done();
-    if ((st = from_cuda(e)) != MLPB_OK) return st;
+    st = from_cuda(e);
   }
 
-  // ---- dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
-  {
-    GemmParams p = base_params(h);
-    p.M = static_cast<int>(H);
-    p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
-    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
-    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
-    p.num_kb = static_cast<int>(T / kBK);
-    p.out0 = dW2;
-    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
-                               static_cast<uint64_t>(t)};
-    const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
-    const uint32_t bbox[3] = {64, kBK, 1};
-    if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
-      return MLPB_EINVAL;
-    st = run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s, "wgrad_w2", 2.0 * H * F * T,
-                  2.0 * (T * H + T * F) + 4.0 * H * F);
-    if (st != MLPB_OK) return st;
-  }
-
-  // ---- dW1 = dZ^T X  (M = F1, N = H, K = T)
-  {
+  // ---- [s2] dW1 = dZ^T X  (M = F1, N = H, K = T)
+  if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(F1);
     p.num_m_tiles = static_cast<int>(cdiv(F1, kBM));
@@ -472,14 +498,14 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
     if (!map2d(&ta, dZ, F1, T, F1, 64, kBK) || !map2d(&tb, X, H, T, H, 64, kBK))
-      return MLPB_EINVAL;
-    st = run_gemm(h, GemmKind::WGRAD_W1, false, ta, tb, p, s, "wgrad_w1", 2.0 * F1 * H * T,
-                  2.0 * (T * F1 + T * H) + 4.0 * F1 * H);
-    if (st != MLPB_OK) return st;
+      st = MLPB_EINVAL;
+    else
+      st = run_gemm(h, GemmKind::WGRAD_W1, false, ta, tb, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
+                    2.0 * (T * F1 + T * H) + 4.0 * F1 * H);
   }
 
-  // ---- dX = sum_i dZ_i W1_i  (f backward: the sum over shards is the K loop)
-  {
+  // ---- [s] dX = sum_i dZ_i W1_i  (f backward: the sum over shards is the K loop)
+  if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(T);
     p.num_m_tiles = static_cast<int>(T / kBM);
@@ -487,10 +513,16 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
     if (!map2d(&ta, dZ, F1, T, F1, kBK, kBM) || !map2d(&tb, W1, H, F1, H, 64, kBK))
-      return MLPB_EINVAL;
-    st = run_gemm(h, GemmKind::DX, false, ta, tb, p, s, "dgrad_x", 2.0 * T * H * F1,
-                  2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+      st = MLPB_EINVAL;
+    else
+      st = run_gemm(h, GemmKind::DX, false, ta, tb, p, s, "dgrad_x", 2.0 * T * H * F1,
+                    2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
   }
+
+  // Join: the caller's stream waits for s2 whatever happened above.
+  if (cudaEventRecord(h->ev_join, s2) != cudaSuccess ||
+      cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess)
+    return MLPB_ECUDA;
   return st;
 }
 

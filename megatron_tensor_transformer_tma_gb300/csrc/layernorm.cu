@@ -6,9 +6,9 @@
 // of the row (kVpt vectors), so every global store is coalesced.  256-thread CTAs, two
 // or more per SM, so that several rows' reduction chains overlap on every SM.
 //
-// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row each thread
-// takes the exact mean and sum of squared deviations of its register-resident values and
-// one block reduction merges them (biased variance); Xn = (x - mu) rstd gamma + beta.
+// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row one block
+// reduction of shifted sums gives the mean and the biased variance of the
+// register-resident row; Xn = (x - mu) rstd gamma + beta in bf16.
 // Sequence shard s owns rows [s T/t, (s+1) T/t); rows are independent, so the forward
 // needs no shard structure and the emulated all-gather is the row layout of Xn itself.
 //
@@ -78,21 +78,11 @@ __device__ __forceinline__ void st_f32x8(float* p, const float* o) {
 }
 
 // ------------------------------------------------------------------ forward
-// Per thread: exact mean and M2 = sum (x - mean)^2 of its own register-resident values;
-// per CTA: one reduction merging the (count, mean, M2) triples of the threads in a fixed
-// order (Chan et al.'s pairwise update), so each row needs a single block reduction.
-__device__ __forceinline__ void chan_merge(float& n, float& m, float& m2, float nb, float mb,
-                                           float m2b) {
-  const float nn = n + nb;
-  if (nn > 0.f) {
-    const float d = mb - m;
-    const float f = nb / nn;
-    m += d * f;
-    m2 += m2b + d * d * n * f;
-    n = nn;
-  }
-}
-
+// Statistics from one pass of shifted sums: with K = the row's first element,
+// S1 = sum (x - K) and S2 = sum (x - K)^2 give mean = K + S1/H and the biased variance
+// S2/H - (S1/H)^2.  Shifting by a value of the row keeps the subtraction well conditioned
+// (the textbook "shifted data" variance), and it needs a single block reduction and about
+// six instructions per element, which is what keeps this kernel memory-bound.
 template <int kVpt>
 __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
@@ -100,15 +90,14 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnFwdThreads;
-  constexpr int NW = NT / 32;
-  __shared__ float shn[NW], shm[NW], shq[NW];
+  __shared__ float sh[2 * NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int64_t n_mine = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
   const WaitCtx wc{&abort_flag, err, wait_ns};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float inv_h = 1.0f / static_cast<float>(H);
 
   if (threadIdx.x == 0) {
     abort_flag = 0u;
@@ -120,18 +109,17 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       bulk_load(buf0 + b * row_bytes, X + row * H, row_bytes, bar0 + 8 * b);
     }
   }
-  // gamma and beta stay packed (bf16) in registers for the whole kernel
-  uint4 gpk[kVpt], bpk[kVpt];
-  int nvalid = 0;
+  float gm[kVpt][8], bt[kVpt][8];
 #pragma unroll
   for (int k = 0; k < kVpt; ++k) {
     const int c = (threadIdx.x + k * NT) * 8;
-    gpk[k] = bpk[k] = make_uint4(0, 0, 0, 0);
+    uint4 g = make_uint4(0, 0, 0, 0), b = g;
     if (c < H) {
-      gpk[k] = ld_global_nc_v4(gamma + c);
-      bpk[k] = ld_global_nc_v4(beta + c);
-      nvalid += 8;
+      g = ld_global_nc_v4(gamma + c);
+      b = ld_global_nc_v4(beta + c);
     }
+    bf16x8_to_f32(g, gm[k]);
+    bf16x8_to_f32(b, bt[k]);
   }
   __syncthreads();
 
@@ -142,43 +130,26 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     int ok = wait_bounded(bar0 + 8 * b, par, wc, kSiteLnFull) ? 1 : 0;
     if (!__syncthreads_and(ok)) break;
     const int64_t row = blockIdx.x + i * gridDim.x;
+    const float K = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ln_smem + b * row_bytes));
     float v[kVpt][8];
-    float sum = 0.f;
+    float s[2] = {0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int vi = threadIdx.x + k * NT;
+      const bool in = vi * 8 < H;
       uint4 u = make_uint4(0, 0, 0, 0);
-      if (vi * 8 < H) u = ld_shared_v4(b * row_bytes + vi * 16);
+      if (in) u = ld_shared_v4(b * row_bytes + vi * 16);
       bf16x8_to_f32(u, v[k]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum += v[k][e];
-    }
-    // this thread's exact (count, mean, M2)
-    float n = static_cast<float>(nvalid);
-    float m = nvalid ? sum / n : 0.f;
-    float m2 = 0.f;
-#pragma unroll
-    for (int k = 0; k < kVpt; ++k)
-      if ((threadIdx.x + k * NT) * 8 < H)
+      if (in) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float d = v[k][e] - m;
-          m2 += d * d;
+          const float d = v[k][e] - K;
+          s[0] += d;
+          s[1] = fmaf(d, d, s[1]);
         }
-    // merge across the warp, then across warps in warp order
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float nb = __shfl_xor_sync(0xffffffffu, n, o);
-      const float mb = __shfl_xor_sync(0xffffffffu, m, o);
-      const float qb = __shfl_xor_sync(0xffffffffu, m2, o);
-      chan_merge(n, m, m2, nb, mb, qb);
+      }
     }
-    if (lane == 0) {
-      shn[warp] = n;
-      shm[warp] = m;
-      shq[warp] = m2;
-    }
-    __syncthreads();  // also: every thread has read buffer b
+    block_sum<NT, 2>(s, sh);  // every thread has read buffer b once this returns
     if (threadIdx.x == 0 && issued < n_mine) {
       const int64_t nrow = blockIdx.x + issued * gridDim.x;
       fence_proxy_async_smem();
@@ -186,22 +157,18 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       bulk_load(buf0 + b * row_bytes, X + nrow * H, row_bytes, bar0 + 8 * b);
     }
     ++issued;
-    float N = shn[0], mu = shm[0], M2 = shq[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) chan_merge(N, mu, M2, shn[w], shm[w], shq[w]);
-    const float r = rsqrtf(M2 / static_cast<float>(H) + eps);
+    const float m1 = s[0] * inv_h;
+    const float var = fmaxf(fmaf(-m1, m1, s[1] * inv_h), 0.f);
+    const float mu = K + m1;
+    const float r = rsqrtf(var + eps);
+    const float c0 = -mu * r;
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int c = (threadIdx.x + k * NT) * 8;
       if (c >= H) continue;
-      float gm[8], bt[8], o[8];
-      bf16x8_to_f32(gpk[k], gm);
-      bf16x8_to_f32(bpk[k], bt);
+      float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float a = r * gm[e];
-        o[e] = fmaf(v[k][e] - mu, a, bt[e]);
-      }
+      for (int e = 0; e < 8; ++e) o[e] = fmaf(fmaf(v[k][e], r, c0), gm[k][e], bt[k][e]);
       st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
     }
@@ -209,7 +176,6 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       mean[row] = mu;
       rstd[row] = r;
     }
-    __syncthreads();  // shn/shm/shq are rewritten by the next row
   }
   // Copies still in flight (only after an abort) must land before the CTA exits.
   if (threadIdx.x == 0 && abort_flag) {
@@ -348,7 +314,7 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
 // ------------------------------------------------------------------ launchers
 static int ln_vpt(int64_t H, int threads) {
   const int64_t v = (H / 8 + threads - 1) / threads;
-  return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : v <= 8 ? 8 : 16;
+  return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : 8;  // H <= 16384
 }
 
 template <class K>
@@ -389,7 +355,6 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
     MLPB_LN_FWD(2)
     MLPB_LN_FWD(4)
     MLPB_LN_FWD(8)
-    MLPB_LN_FWD(16)
 #undef MLPB_LN_FWD
   }
   if (e != cudaSuccess) return e;
