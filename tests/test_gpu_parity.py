@@ -78,7 +78,8 @@ def test_layernorm_sp_components():
     # Xn is bf16: within one bf16 rounding of the oracle plus 1e-3 RMS
     got = to_f64(Xn)
     assert np.all(np.abs(got - rXn) <= np.abs(rXn) * 2.0 ** -8 + 1e-3 * np.sqrt(np.mean(rXn ** 2)))
-    compare("mean", to_f64(mean), rmu, tol=1e-5)
+    # the mean is judged on the scale of the data it averages (rows have std ~1)
+    assert np.abs(to_f64(mean) - rmu).max() <= 1e-5 * np.sqrt(np.mean(x64 ** 2))
     compare("rstd", to_f64(rstd), rrs, tol=1e-5)
     rdX, rdg, rdb = oln.layernorm_sp_bwd(x64, g64, rmu, rrs, to_f64(dXn), 8)
     compare("ln_dX", to_f64(dX), rdX, tol=1e-4)
