@@ -166,7 +166,9 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle *h, const void *X, const void *gam
  * the stream reported an error, else MLPB_OK. */
 mlpb_status mlpb_last_device_error(mlpb_handle *h, mlpb_stream_t stream);
 
-/* Enables (1) or disables (0) per-kernel CUDA-event timing on the handle. */
+/* Enables (1) or disables (0) per-kernel CUDA-event timing on the handle.  While it is
+ * on, mlpb_backward issues all of its kernels on the caller's stream, one after the other,
+ * so that every recorded interval belongs to one kernel. */
 mlpb_status mlpb_enable_timing(mlpb_handle *h, int enable);
 
 /* Copies up to `capacity` timing records of the launches since the last read

@@ -40,7 +40,7 @@ mlpb_status load_encoder() {
   return MLPB_OK;
 }
 
-// A bf16 tensor map with 128-byte swizzle.  dims[0] is the contiguous dimension;
+// A bf16 tensor map with the swizzle matching its box row.  dims[0] is contiguous;
 // strides_bytes[k] is the byte stride of dimension k+1.
 bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box) {
@@ -52,10 +52,12 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
     es[k] = 1;
     if (k + 1 < rank) gs[k] = strides_bytes[k];
   }
+  // the swizzle span is the box's innermost row: 128 B (64 bf16) or 64 B (32 bf16)
+  const CUtensorMapSwizzle sw =
+      box[0] * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
                         const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -420,7 +422,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
   float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
                                           align256(static_cast<size_t>(h->db2_splits) * H * 4));
-  cudaStream_t s2 = h->side;
+  // With per-kernel timing on, everything stays on `stream`, so that each kernel's
+  // CUDA-event interval is its own and not shared with a concurrent one.
+  cudaStream_t s2 = h->timing ? s : h->side;
 
   // Fork: stream s2 starts with everything that needs only dY and A.
   if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||

@@ -4,8 +4,8 @@
 // of a pair compute M tiles 2p and 2p+1 against the same N tile, so each loads its own A
 // tile and HALF of the shared B tile, multicasting that half into both CTAs' shared
 // memory (a third fewer L2->SM bytes per CTA than loading B alone).
-//   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
-//               (128-byte swizzle) and arms the stage's mbarrier with the byte count;
+//   warp 0      TMA producer: fills an 8-stage ring of 128x32 A and 256x32 B bf16 tiles
+//               (swizzled) and arms the stage's mbarrier with the byte count;
 //   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
 //               N=256, K=16) from one thread into one of two 256-column fp32
 //               accumulators, committing each consumed stage back to the producers of
@@ -459,12 +459,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = sA0 + stage * kAStage;
           const uint32_t sb = sB0 + stage * kBStage;
+          // K-major: 16 K elements = 32 bytes further along the row; MN-major: 16 K rows
+          // of 128 bytes further down the chunk.
+          constexpr uint32_t kKSw = kKRowBytes == 128 ? 2u : 4u;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = KindOf<K>::a_mn ? sdesc_sw128(sa + kk * 2048, kChunk, 1024)
-                                                : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = KindOf<K>::b_mn ? sdesc_sw128(sb + kk * 2048, kChunk, 1024)
-                                                : sdesc_sw128(sb + kk * 32, 16, 1024);
+            const uint64_t ad = KindOf<K>::a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
+                                                : sdesc(sa + kk * 32, 16, 8 * kKRowBytes, kKSw);
+            const uint64_t bd = KindOf<K>::b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
+                                                : sdesc(sb + kk * 32, 16, 8 * kKRowBytes, kKSw);
             umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           if constexpr (CM > 1) umma_commit_mc(empty0 + 8 * stage, kPairMask);

@@ -211,20 +211,21 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
+// Shared-memory matrix descriptor of a swizzled operand tile.
 //   bits 0-13  start address >> 4        bits 16-29 leading-dimension byte offset >> 4
 //   bits 32-45 stride-dimension byte offset >> 4
-//   bits 46-48 fixed 0b001               bits 61-63 swizzle mode (2 = 128 B)
-// K-major tiles: rows of 128 B (64 bf16 of K), 8-row groups `sbo` bytes apart, LBO unused.
-// MN-major tiles: rows of 128 B (64 bf16 of M or N) per K index, 8-K-row groups `sbo`
-// bytes apart, 64-wide M/N chunks `lbo` bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   bits 46-48 fixed 0b001               bits 61-63 swizzle mode (2 = 128 B, 4 = 64 B)
+// K-major tiles: rows of one k-block (64 or 128 B), 8-row groups `sbo` bytes apart, LBO
+// unused.  MN-major tiles (128-byte swizzle): rows of 64 M/N elements per K index,
+// 8-K-row groups `sbo` bytes apart, 64-wide M/N chunks `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                          uint32_t swizzle_mode) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= static_cast<uint64_t>(swizzle_mode & 7u) << 61;
   return d;
 }
 
