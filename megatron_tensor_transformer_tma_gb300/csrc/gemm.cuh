@@ -4,10 +4,8 @@
 // of a pair compute M tiles 2p and 2p+1 against the same N tile, so each loads its own A
 // tile and HALF of the shared B tile, multicasting that half into both CTAs' shared
 // memory (a third fewer L2->SM bytes per CTA than loading B alone).
-//   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
-//               (128-byte swizzle) and arms the stage's mbarrier with the byte count; it
-//               also asks L2 to prefetch the tiles kPrefetchKb k-blocks ahead, so that
-//               first touches from HBM overlap the MMAs of the stages in flight;
+//   warp 0      TMA producer: fills an 8-stage ring of 128x32 A and 256x32 B bf16 tiles
+//               (swizzled) and arms the stage's mbarrier with the byte count;
 //   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
 //               N=256, K=16) from one thread into one of two 256-column fp32
 //               accumulators, committing each consumed stage back to the producers of
@@ -56,78 +54,80 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   nt = r / gm;
 }
 
-// One box of a stage.  PF: only prefetch it into L2.  MC: multicast it to both CTAs of
-// the pair (when CM == 2).  Otherwise a plain load into this CTA's shared memory.
-template <int CM, bool PF, bool MC>
-__device__ __forceinline__ void box2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+// TMA loads that multicast to both CTAs of the pair when CM == 2.
+template <int CM>
+__device__ __forceinline__ void tma2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
                                      int c1) {
-  if constexpr (PF) tma_prefetch_2d(m, c0, c1);
-  else if constexpr (MC && CM == 2) tma_load_2d_mc(dst, m, bar, c0, c1, 0x3);
-  else tma_load_2d(dst, m, bar, c0, c1);
+  if constexpr (CM == 1) tma_load_2d(dst, m, bar, c0, c1);
+  else tma_load_2d_mc(dst, m, bar, c0, c1, static_cast<uint16_t>((1u << CM) - 1));
 }
-template <int CM, bool PF, bool MC>
-__device__ __forceinline__ void box3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+template <int CM>
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
                                      int c1, int c2) {
-  if constexpr (PF) tma_prefetch_3d(m, c0, c1, c2);
-  else if constexpr (MC && CM == 2) tma_load_3d_mc(dst, m, bar, c0, c1, c2, 0x3);
-  else tma_load_3d(dst, m, bar, c0, c1, c2);
+  if constexpr (CM == 1) tma_load_3d(dst, m, bar, c0, c1, c2);
+  else tma_load_3d_mc(dst, m, bar, c0, c1, c2, static_cast<uint16_t>((1u << CM) - 1));
 }
-template <int CM, bool PF, bool MC>
-__device__ __forceinline__ void box4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+template <int CM>
+__device__ __forceinline__ void tma4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
                                      int c1, int c2, int c3) {
-  if constexpr (PF) tma_prefetch_4d(m, c0, c1, c2, c3);
-  else if constexpr (MC && CM == 2) tma_load_4d_mc(dst, m, bar, c0, c1, c2, c3, 0x3);
-  else tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  if constexpr (CM == 1) tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  else tma_load_4d_mc(dst, m, bar, c0, c1, c2, c3, static_cast<uint16_t>((1u << CM) - 1));
 }
 
 // One stage: this CTA's own A tile, and the B pieces this CTA owns.  B is two 128-row
 // K-major pieces (16 KB) or four 64-wide MN-major chunks (8 KB); with CM = 2 the CTA of
-// rank r loads pieces r (or chunks 2r, 2r+1) and multicasts them to both CTAs.  With PF
-// the same boxes are only prefetched into L2.
-template <GemmKind K, int CM, bool PF>
+// rank r loads pieces r (or chunks 2r, 2r+1) and multicasts them to both CTAs.
+template <GemmKind K, int CM>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tA, const CUtensorMap* tB,
                                             uint32_t sa, uint32_t sb, uint32_t bar, int mt,
                                             int nt, int kb, int rank, const GemmParams& p) {
   const int k0 = kb * kBK;
-  constexpr int kPieces = (K == GemmKind::FC1_GELU || K == GemmKind::FC1_SWIGLU ||
-                           K == GemmKind::FC2) ? 2 : 4;
-  const int q0 = CM == 2 ? rank * (kPieces / 2) : 0;
-  const int q1 = CM == 2 ? q0 + kPieces / 2 : kPieces;
   if constexpr (K == GemmKind::FC1_GELU) {
-    box2<CM, PF, false>(sa, tA, bar, k0, mt * kBM);
-    for (int q = q0; q < q1; ++q)
-      box2<CM, PF, true>(sb + q * (kBStage / 2), tB, bar, k0, nt * kBN + 128 * q);
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma2<CM>(sb + q * (kBStage / 2), tB, bar, k0, nt * kBN + 128 * q);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * 128;
-    box2<CM, PF, false>(sa, tA, bar, k0, mt * kBM);
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
     // piece 0: gate rows -> B rows 0..127; piece 1: up rows -> B rows 128..255
-    for (int q = q0; q < q1; ++q)
-      box4<CM, PF, true>(sb + q * (kBStage / 2), tB, bar, k0, j0, q, i);
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma4<CM>(sb + q * (kBStage / 2), tB, bar, k0, j0, q, i);
   } else if constexpr (K == GemmKind::FC2) {
     const int i = kb / p.kb_per_shard;
     const int j0 = (kb - i * p.kb_per_shard) * kBK;
-    box3<CM, PF, false>(sa, tA, bar, j0, mt * kBM, i);
-    for (int q = q0; q < q1; ++q)
-      box3<CM, PF, true>(sb + q * (kBStage / 2), tB, bar, j0, nt * kBN + 128 * q, i);
+    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
+#pragma unroll
+    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
+      tma3<CM>(sb + q * (kBStage / 2), tB, bar, j0, nt * kBN + 128 * q, i);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
-    box2<CM, PF, false>(sa, tA, bar, k0, mt * kBM);
-    for (int q = q0; q < q1; ++q) box3<CM, PF, true>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
   } else if constexpr (K == GemmKind::DX) {
-    box2<CM, PF, false>(sa, tA, bar, k0, mt * kBM);
-    for (int q = q0; q < q1; ++q) box2<CM, PF, true>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
   } else if constexpr (K == GemmKind::WGRAD_W2) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) box2<CM, PF, false>(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
-    for (int q = q0; q < q1; ++q) box3<CM, PF, true>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
   } else {  // WGRAD_W1
 #pragma unroll
-    for (int q = 0; q < 2; ++q) box2<CM, PF, false>(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
-    for (int q = q0; q < q1; ++q) box2<CM, PF, true>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
+      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
   }
 }
 
@@ -410,8 +410,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int mp, nt;
         tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * CM + rank;
-        for (int kb = 0; kb < kPrefetchKb && kb < p.num_kb; ++kb)
-          issue_stage<K, CM, true>(&tmA, &tmB, 0, 0, 0, mt, nt, kb, rank, p);
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
@@ -423,10 +421,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, kStageBytes);
-            issue_stage<K, CM, false>(&tmA, &tmB, sA0 + stage * kAStage,
-                                      sB0 + stage * kBStage, fb, mt, nt, kb, rank, p);
-            if (kb + kPrefetchKb < p.num_kb)
-              issue_stage<K, CM, true>(&tmA, &tmB, 0, 0, 0, mt, nt, kb + kPrefetchKb, rank, p);
+            issue_stage<K, CM>(&tmA, &tmB, sA0 + stage * kAStage, sB0 + stage * kBStage, fb, mt,
+                               nt, kb, rank, p);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
