@@ -4,8 +4,8 @@
 // of a pair compute M tiles 2p and 2p+1 against the same N tile, so each loads its own A
 // tile and HALF of the shared B tile, multicasting that half into both CTAs' shared
 // memory (a third fewer L2->SM bytes per CTA than loading B alone).
-//   warp 0      TMA producer: fills an 8-stage ring of 128x32 A and 256x32 B bf16 tiles
-//               (swizzled) and arms the stage's mbarrier with the byte count;
+//   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
+//               (128-byte swizzle) and arms the stage's mbarrier with the byte count;
 //   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
 //               N=256, K=16) from one thread into one of two 256-column fp32
 //               accumulators, committing each consumed stage back to the producers of

@@ -19,12 +19,12 @@ enum class GemmKind : int {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 32;      // k-block depth: 32 bf16 = 64-byte K-major rows
-constexpr int kStages = 8;   // 8 x 24 KB ring: refills released every two MMAs
-constexpr int kAStage = kBM * kBK * 2;  // 8 KB
-constexpr int kBStage = kBN * kBK * 2;  // 16 KB
+constexpr int kBK = 64;     // k-block depth: 64 bf16 = 128-byte K-major rows
+constexpr int kStages = 4;  // 4 x 48 KB ring (32-deep blocks in 8 stages measured slower)
+constexpr int kAStage = kBM * kBK * 2;  // 16 KB
+constexpr int kBStage = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x kBK(K) MN-major box, 4 KB
+constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x kBK(K) MN-major box, 8 KB
 // K-major tiles use the swizzle whose row is one k-block (64 B for kBK = 32), MN-major
 // tiles the 128-byte swizzle (rows of 64 M/N elements).
 constexpr int kKRowBytes = kBK * 2;
