@@ -18,6 +18,8 @@ enum WaitSite : uint32_t {
   kSiteEpiAccFull = 4,
   kSiteDrain = 5,
   kSiteLnFull = 6,
+  kSiteRelay = 7,
+  kSitePeerFull = 8,
 };
 
 // Default limit of one bounded wait: 1 s of wall time (globaltimer).
@@ -37,6 +39,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort_flag = 1u;
+        atomicCAS(w.err, 0u, kDevErrTimeout | site);
+        return false;
+      }
+    }
+  }
+}
+
+// wait_bounded for a phase completed by arrivals from another CTA of the cluster.
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     const WaitCtx& w, uint32_t site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*w.abort_flag) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {

@@ -520,4 +520,259 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ======================================================================================
+// CTA-pair kernel.  The two CTAs of a cluster run one tcgen05.mma.cta_group::2 stream:
+// M = 256 (each CTA's 128 A rows and 128 TMEM lanes), N = 256 (each CTA's shared memory
+// holds one 128-row half of B), so every B byte in shared memory feeds both SMs' tensor
+// cores.  Per SM and per 64-deep k-block that is 32 KB written by TMA and 32 KB read by the
+// tensor core, against 48 + 48 KB for one CTA computing a 128 x 256 tile alone.
+//   warp 0 (both CTAs)  TMA producer for this CTA's A rows and B half, on its own barrier;
+//   warp 1 (even CTA)   allocates TMEM with its peer and issues the pair's MMAs;
+//   warp 1 (odd CTA)    allocates TMEM with its peer and relays "stage s has landed here"
+//                       to the even CTA (a remote mbarrier arrive);
+//   warps 2..5          epilogue of this CTA's 128 rows, releasing the accumulator to the
+//                       even CTA's MMA issuer.
+// ======================================================================================
+template <GemmKind K>
+__device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CUtensorMap* tB,
+                                                 uint32_t sa, uint32_t sb, uint32_t bar, int mt,
+                                                 int nt, int kb, int rank,
+                                                 const GemmParams& p) {
+  const int k0 = kb * kBK;
+  const int nh = nt * kBN + 128 * rank;  // first B row (N index) of this CTA's half
+  if constexpr (K == GemmKind::FC1_GELU) {
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_2d(sb, tB, bar, k0, nh);
+  } else if constexpr (K == GemmKind::FC1_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * 128;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_4d(sb, tB, bar, k0, j0, rank, i);  // even CTA: gate rows, odd CTA: up rows
+  } else if constexpr (K == GemmKind::FC2) {
+    const int i = kb / p.kb_per_shard;
+    const int j0 = (kb - i * p.kb_per_shard) * kBK;
+    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
+    tma_load_3d(sb, tB, bar, j0, nh, i);
+  } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+  } else if constexpr (K == GemmKind::DX) {
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+  } else if constexpr (K == GemmKind::WGRAD_W2) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+  } else {  // WGRAD_W1
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+  }
+}
+
+template <GemmKind K>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  constexpr int S = kPairStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + S * kPairAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const uint32_t full0 = smem_u32(bars);            // this CTA's TMA landed
+  const uint32_t pfull0 = smem_u32(bars + S);       // even CTA: the odd CTA's TMA landed
+  const uint32_t empty0 = smem_u32(bars + 2 * S);   // the pair's MMAs have read stage s
+  const uint32_t tfull0 = smem_u32(bars + 3 * S);
+  const uint32_t tempty0 = smem_u32(bars + 3 * S + 2);
+  const uint32_t drain = smem_u32(bars + 3 * S + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x / 2;
+  const int nclusters = gridDim.x / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(pfull0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t pfull_lead = mapa_shared(pfull0, 0);
+  const uint32_t tempty_lead = mapa_shared(tempty0, 0);
+
+  const WaitCtx wc{abort_flag, p.err, p.wait_ns};
+  const int num_pm = (p.num_m_tiles + 1) / 2;
+  const int num_super = num_pm * p.num_n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool skip_once = p.fault_inject != 0 && cid == 0 && leader;
+      for (int st = cid; st < num_super; st += nclusters) {
+        int mp, nt;
+        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
+        const int mt = mp * 2 + rank;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded_cluster(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (skip_once) {
+            skip_once = false;  // fault injection: this stage is never armed
+          } else {
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, kPairStageBytes);
+            issue_stage_pair<K>(&tmA, &tmB, sA0 + stage * kPairAStage, sB0 + stage * kPairBStage,
+                                fb, mt, nt, kb, rank, p);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) wait_drain(full0 + 8 * s, (armed_par >> s) & 1u, wc);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA issuer (pair)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, KindOf<K>::a_mn, KindOf<K>::b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int st = cid; st < num_super; st += nclusters, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!wait_bounded_cluster(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull) ||
+              !wait_bounded_cluster(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sA0 + stage * kPairAStage;
+          const uint32_t sb = sB0 + stage * kPairBStage;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = KindOf<K>::a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
+                                                : sdesc(sa + kk * 32, 16, 1024, 2u);
+            const uint64_t bd = KindOf<K>::b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
+                                                : sdesc(sb + kk * 32, 16, 1024, 2u);
+            umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_mc(empty0 + 8 * stage, 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(tfull0 + 8 * buf, 0x3);
+      }
+      umma_commit_pair(drain);
+      wait_drain(drain, 0, wc);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------------- relay (odd CTA)
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int st = cid; st < num_super; st += nclusters) {
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteRelay)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(pfull_lead + 8 * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int st = cid; st < num_super; st += nclusters, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_bounded_cluster(tfull0 + 8 * buf, acc_par, wc, kSiteEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after();
+      int mp, nt;
+      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
+      epilogue_tile<K>(tacc, row, mp * 2 + rank, nt, p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty0 + 8 * buf);
+        else mbar_arrive_remote(tempty_lead + 8 * buf);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // no remote arrive or MMA of the pair is still outstanding
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace mlpb

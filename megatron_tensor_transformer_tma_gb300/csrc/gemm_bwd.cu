@@ -7,8 +7,8 @@ namespace mlpb {
 
 template <GemmKind K>
 static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gemm_kernel<K, kClusterM>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  return cudaFuncSetAttribute(gemm_pair_kernel<K>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
 }
 
 // `clusters` clusters of kClusterM CTAs, one CTA per SM.
@@ -18,7 +18,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kClusterM), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -27,7 +27,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<K, kClusterM>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<K>, a, b, p);
 }
 
 cudaError_t gemm_bwd_set_smem_attrs() {

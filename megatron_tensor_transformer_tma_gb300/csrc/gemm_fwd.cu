@@ -6,8 +6,8 @@ namespace mlpb {
 
 template <GemmKind K>
 static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gemm_kernel<K, kClusterM>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  return cudaFuncSetAttribute(gemm_pair_kernel<K>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
 }
 
 // `clusters` clusters of kClusterM CTAs, one CTA per SM.
@@ -17,7 +17,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kClusterM), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -26,7 +26,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<K, kClusterM>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<K>, a, b, p);
 }
 
 cudaError_t gemm_fwd_set_smem_attrs() {
@@ -56,7 +56,7 @@ cudaError_t gemm_max_active_clusters(int* out) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kClusterM, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.dynamicSmemBytes = kPairSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterM;
@@ -64,7 +64,7 @@ cudaError_t gemm_max_active_clusters(int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, gemm_kernel<GemmKind::FC1_GELU, kClusterM>, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, gemm_pair_kernel<GemmKind::FC1_GELU>, &cfg);
 }
 
 }  // namespace mlpb
