@@ -50,24 +50,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
-// wait_bounded for a phase completed by arrivals from another CTA of the cluster.
-__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
-                                                     const WaitCtx& w, uint32_t site) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 63u) == 0u) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        *w.abort_flag = 1u;
-        atomicCAS(w.err, 0u, kDevErrTimeout | site);
-        return false;
-      }
-    }
-  }
-}
-
 // Waits for copies or MMAs that were already issued (they always complete); ignores the
 // abort flag but still gives up after the limit.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {

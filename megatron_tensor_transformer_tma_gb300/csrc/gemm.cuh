@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int mt = mp * 2 + rank;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bounded_cluster(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
@@ -685,13 +685,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int st = cid; st < num_super; st += nclusters, ++it) {
         const int buf = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
-        if (!wait_bounded_cluster(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
+        if (!wait_bounded(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull) ||
-              !wait_bounded_cluster(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
+              !wait_bounded(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
             ok = false;
             break;
           }
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t acc_par = (it >> 1) & 1;
       int ok = 1;
       if (lane == 0)
-        ok = wait_bounded_cluster(tfull0 + 8 * buf, acc_par, wc, kSiteEpiAccFull) ? 1 : 0;
+        ok = wait_bounded(tfull0 + 8 * buf, acc_par, wc, kSiteEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
