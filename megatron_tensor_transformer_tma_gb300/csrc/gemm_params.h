@@ -36,13 +36,11 @@ constexpr int kClusterM = 2;  // CTAs per cluster (a pair along M)
 
 // CTA-pair (cta_group::2) variant: a pair computes a 256 x 256 tile; each CTA keeps its
 // 128 rows of A and its 128-row half of B per stage, so a stage is 32 KB per CTA.
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 7;
 constexpr int kPairAStage = kBM * kBK * 2;         // 16 KB
 constexpr int kPairBStage = (kBN / 2) * kBK * 2;   // 16 KB
 constexpr int kPairStageBytes = kPairAStage + kPairBStage;
-// + 32 KB of slack past the barriers, so that no descriptor of the ring can address
-// beyond the CTA's shared-memory allocation
-constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + 512 + 32768;
+constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + 512;  // 225.5 KB
 
 struct GemmParams {
   int num_m_tiles, num_n_tiles, num_kb;
