@@ -154,20 +154,6 @@ GemmParams base_params(const mlpb_handle* h) {
   return p;
 }
 
-// Raster order of one GEMM.  A pair tile reads a 256 x K panel of each operand; keeping
-// `G` panels of one operand resident (about 48 MB of the 129 MB L2) while the other streams
-// past them reads the resident operand once and the streaming one ceil(tiles / G) times.
-// The direction with fewer bytes from HBM wins.
-void plan_raster(GemmParams& p, int64_t K, double a_bytes, double b_bytes) {
-  const int num_pm = static_cast<int>(cdiv(p.num_m_tiles, kClusterM));
-  const double panel = 256.0 * static_cast<double>(K) * 2.0;
-  const int G = static_cast<int>(std::max<double>(1.0, std::floor((48.0 * (1 << 20)) / panel)));
-  const double along_m = a_bytes + b_bytes * static_cast<double>(cdiv(num_pm, G));
-  const double along_n = b_bytes + a_bytes * static_cast<double>(cdiv(p.num_n_tiles, G));
-  p.raster_group = G;
-  p.raster_along_n = along_n < along_m ? 1 : 0;
-}
-
 mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap& a,
                      const CUtensorMap& b, const GemmParams& p, cudaStream_t s, const char* name,
                      double flops, double bytes) {
@@ -362,7 +348,6 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
     if (!map2d(&tb, W1, H, F, H, kBK, kBN / 2)) return MLPB_EINVAL;
     p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
     p.bias = static_cast<const __nv_bfloat16*>(b1);
-    plan_raster(p, H, 2.0 * T * H, 2.0 * F * H);
     st = run_gemm(h, GemmKind::FC1_GELU, true, ta, tb, p, s, "fc1_gelu", 2.0 * T * F * H,
                   2.0 * (T * H + F * H + 2 * T * F) + (bias ? 2.0 * F : 0.0));
   } else {
@@ -374,7 +359,6 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
     if (!encode_bf16(&tb, W1, 4, dims, str, box)) return MLPB_EINVAL;
     p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
     p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
-    plan_raster(p, H, 2.0 * T * H, 4.0 * F * H);
     st = run_gemm(h, GemmKind::FC1_SWIGLU, true, ta, tb, p, s, "fc1_swiglu", 4.0 * T * F * H,
                   2.0 * (T * H + 2 * F * H + 3 * T * F));
   }
@@ -400,7 +384,6 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
     q.num_kb = static_cast<int>(t * q.kb_per_shard);
     q.bias = static_cast<const __nv_bfloat16*>(b2);
     q.out0 = Y;
-    plan_raster(q, F, 2.0 * T * F, 2.0 * H * F);
     st = run_gemm(h, GemmKind::FC2, true, ta, tb, q, s, "fc2", 2.0 * T * H * F,
                   2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0));
   }
@@ -470,7 +453,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
     const uint32_t bbox[3] = {64, kBK, 1};
-    plan_raster(p, T, 2.0 * T * H, 2.0 * T * F);
     if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
       st = MLPB_EINVAL;
     else
@@ -492,7 +474,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
     const uint32_t bbox[3] = {64, kBK, 1};
-    plan_raster(p, H, 2.0 * T * H, 2.0 * F * H);
     if (!map2d(&ta, dY, H, T, H, kBK, kBM) || !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
       st = MLPB_EINVAL;
     else
@@ -520,7 +501,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
-    plan_raster(p, T, 2.0 * T * F1, 2.0 * T * H);
     if (!map2d(&ta, dZ, F1, T, F1, 64, kBK) || !map2d(&tb, X, H, T, H, 64, kBK))
       st = MLPB_EINVAL;
     else
@@ -536,7 +516,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
-    plan_raster(p, F1, 2.0 * T * F1, 2.0 * F1 * H);
     if (!map2d(&ta, dZ, F1, T, F1, kBK, kBM) || !map2d(&tb, W1, H, F1, H, 64, kBK))
       st = MLPB_EINVAL;
     else

@@ -41,29 +41,17 @@ struct KindOf {
                                 K == GemmKind::WGRAD_W1);
 };
 
-// Grouped rasterisation: `group` consecutive M tiles (or M-tile pairs) sweep all N tiles
-// together, or -- along_n -- `group` N tiles sweep all M tiles, so that the panels of the
-// group stay in L2 while the other operand streams past them once.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group,
-                                            int along_n, int& mt, int& nt) {
-  const int G = group > 0 ? group : 8;
-  if (!along_n) {
-    const int span = G * num_n;
-    const int g = tile / span;
-    const int m0 = g * G;
-    const int gm = min(num_m - m0, G);
-    const int r = tile - g * span;
-    mt = m0 + r % gm;
-    nt = r / gm;
-  } else {
-    const int span = G * num_m;
-    const int g = tile / span;
-    const int n0 = g * G;
-    const int gn = min(num_n - n0, G);
-    const int r = tile - g * span;
-    nt = n0 + r % gn;
-    mt = r / gn;
-  }
+// Grouped rasterisation: 8 consecutive M tiles (or M-tile pairs) sweep all N tiles
+// together so that the B tiles they share stay in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mt, int& nt) {
+  constexpr int G = 8;
+  const int span = G * num_n;
+  const int g = tile / span;
+  const int m0 = g * G;
+  const int gm = min(num_m - m0, G);
+  const int r = tile - g * span;
+  mt = m0 + r % gm;
+  nt = r / gm;
 }
 
 // TMA loads that multicast to both CTAs of the pair when CM == 2.
@@ -420,7 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool skip_once = p.fault_inject != 0 && cid == 0 && rank == 0;
       for (int st = cid; st < num_super; st += nclusters) {
         int mp, nt;
-        tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, p.raster_along_n, mp, nt);
+        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * CM + rank;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -511,7 +499,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       tc_fence_after();
       int mp, nt;
-      tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, p.raster_along_n, mp, nt);
+      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
       epilogue_tile<K>(tacc, row, mp * CM + rank, nt, p);
       tc_fence_before();
@@ -661,7 +649,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool skip_once = p.fault_inject != 0 && cid == 0 && leader;
       for (int st = cid; st < num_super; st += nclusters) {
         int mp, nt;
-        tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, p.raster_along_n, mp, nt);
+        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * 2 + rank;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -767,7 +755,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       tc_fence_after();
       int mp, nt;
-      tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, p.raster_along_n, mp, nt);
+      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
       epilogue_tile<K>(tacc, row, mp * 2 + rank, nt, p);
       tc_fence_before();

@@ -55,8 +55,6 @@ struct GemmParams {
   uint32_t* err;
   uint64_t wait_ns;
   int fault_inject;
-  int raster_group;    // tiles of the grouped dimension that sweep the other one together
-  int raster_along_n;  // 1: groups of N tiles sweep all M tiles; 0: groups of M tiles
 };
 
 }  // namespace mlpb
