@@ -1,25 +1,26 @@
-// Persistent, warp-specialised tcgen05 GEMM for the MLP block's six contractions.
+// Persistent, warp-specialised tcgen05 GEMM for the MLP block's six contractions, run by
+// CTA pairs (clusters of two CTAs on two SMs, tcgen05 cta_group::2).
 //
-// One CTA per SM (192 threads), CTAs paired in clusters of CM = 2 along M: the two CTAs
-// of a pair compute M tiles 2p and 2p+1 against the same N tile, so each loads its own A
-// tile and HALF of the shared B tile, multicasting that half into both CTAs' shared
-// memory (a third fewer L2->SM bytes per CTA than loading B alone).
-//   warp 0      TMA producer: fills a 4-stage ring of 128x64 A and 256x64 B bf16 tiles
-//               (128-byte swizzle) and arms the stage's mbarrier with the byte count;
-//   warp 1      allocates 512 tensor-memory columns and issues tcgen05.mma (M=128,
-//               N=256, K=16) from one thread into one of two 256-column fp32
-//               accumulators, committing each consumed stage back to the producers of
-//               both CTAs of the pair (a stage is refilled only when both have read it);
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp owns the 32 TMEM lanes
-//               of its warp-id modulo 4), apply the fused pointwise op, store to HBM,
-//               then release the accumulator so the next tile's K loop can run.
+// A pair computes a 256 x 256 output tile: M = 256 rows, 128 in each CTA's A tile and TMEM
+// lanes; N = 256 columns, with each CTA's shared memory holding one 128-row half of the B
+// tile, so every B byte in shared memory feeds both SMs' tensor cores.  Each CTA (192
+// threads) has:
+//   warp 0      TMA producer: a 7-stage ring of 128x64 A and 128x64 B-half bf16 tiles
+//               (128-byte swizzle, 32 KB a stage), armed with the byte count;
+//   warp 1      with its peer, allocates 512 TMEM columns (two 256-column fp32
+//               accumulators); in the even CTA it issues the pair's tcgen05.mma (M=256,
+//               N=256, K=16) and commits each consumed stage to both CTAs' producers; in
+//               the odd CTA it relays "this stage has landed here" to the even CTA;
+//   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows (each warp owns the
+//               32 TMEM lanes of its warp-id modulo 4), the fused pointwise op, stores to
+//               HBM, then the accumulator is released to the even CTA's MMA issuer.
 // Every wait is bounded (common.cuh): a wait that expires raises the CTA's abort flag
 // and the device error word; all roles then drain what they issued and free TMEM.
 //
 // The contractions (T tokens, H hidden, F ffn, t shards, Fs = F/t, F1 = F or 2F):
 //   FC1_GELU      Z = X W1^T + b1, A = gelu(Z)       M=T  N=F      K=H   A,B K-major
 //   FC1_SWIGLU    [G|U] = X [Wg_i|Wu_i]^T, A = silu(G)U  (per shard i, 128 gate + 128 up
-//                 columns per tile, one N=256 MMA)    M=T  N=2F     K=H
+//                 columns per tile: the even CTA holds the gate rows, the odd the up rows)
 //   FC2           Y = sum_i A_i W2_i^T + b2           M=T  N=H      K=t x Fs (walks shards)
 //   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B MN-major
 //   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B MN-major
@@ -52,83 +53,6 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   const int r = tile - g * span;
   mt = m0 + r % gm;
   nt = r / gm;
-}
-
-// TMA loads that multicast to both CTAs of the pair when CM == 2.
-template <int CM>
-__device__ __forceinline__ void tma2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                     int c1) {
-  if constexpr (CM == 1) tma_load_2d(dst, m, bar, c0, c1);
-  else tma_load_2d_mc(dst, m, bar, c0, c1, static_cast<uint16_t>((1u << CM) - 1));
-}
-template <int CM>
-__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                     int c1, int c2) {
-  if constexpr (CM == 1) tma_load_3d(dst, m, bar, c0, c1, c2);
-  else tma_load_3d_mc(dst, m, bar, c0, c1, c2, static_cast<uint16_t>((1u << CM) - 1));
-}
-template <int CM>
-__device__ __forceinline__ void tma4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                     int c1, int c2, int c3) {
-  if constexpr (CM == 1) tma_load_4d(dst, m, bar, c0, c1, c2, c3);
-  else tma_load_4d_mc(dst, m, bar, c0, c1, c2, c3, static_cast<uint16_t>((1u << CM) - 1));
-}
-
-// One stage: this CTA's own A tile, and the B pieces this CTA owns.  B is two 128-row
-// K-major pieces (16 KB) or four 64-wide MN-major chunks (8 KB); with CM = 2 the CTA of
-// rank r loads pieces r (or chunks 2r, 2r+1) and multicasts them to both CTAs.
-template <GemmKind K, int CM>
-__device__ __forceinline__ void issue_stage(const CUtensorMap* tA, const CUtensorMap* tB,
-                                            uint32_t sa, uint32_t sb, uint32_t bar, int mt,
-                                            int nt, int kb, int rank, const GemmParams& p) {
-  const int k0 = kb * kBK;
-  if constexpr (K == GemmKind::FC1_GELU) {
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-#pragma unroll
-    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
-      tma2<CM>(sb + q * (kBStage / 2), tB, bar, k0, nt * kBN + 128 * q);
-  } else if constexpr (K == GemmKind::FC1_SWIGLU) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * 128;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    // piece 0: gate rows -> B rows 0..127; piece 1: up rows -> B rows 128..255
-#pragma unroll
-    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
-      tma4<CM>(sb + q * (kBStage / 2), tB, bar, k0, j0, q, i);
-  } else if constexpr (K == GemmKind::FC2) {
-    const int i = kb / p.kb_per_shard;
-    const int j0 = (kb - i * p.kb_per_shard) * kBK;
-    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
-#pragma unroll
-    for (int q = (CM == 2 ? rank : 0); q < (CM == 2 ? rank + 1 : 2); ++q)
-      tma3<CM>(sb + q * (kBStage / 2), tB, bar, j0, nt * kBN + 128 * q, i);
-  } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-#pragma unroll
-    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
-      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
-  } else if constexpr (K == GemmKind::DX) {
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-#pragma unroll
-    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
-      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
-  } else if constexpr (K == GemmKind::WGRAD_W2) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
-#pragma unroll
-    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
-      tma3<CM>(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
-  } else {  // WGRAD_W1
-#pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
-#pragma unroll
-    for (int q = (CM == 2 ? 2 * rank : 0); q < (CM == 2 ? 2 * rank + 2 : 4); ++q)
-      tma2<CM>(sb + q * kChunk, tB, bar, nt * kBN + 64 * q, k0);
-  }
 }
 
 // ------------------------------------------------------------------ pointwise math
@@ -344,197 +268,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
   }
 }
 
-template <GemmKind K, int CM>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sA0 = base;
-  const uint32_t sB0 = base + kStages * kAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
-  constexpr uint16_t kPairMask = static_cast<uint16_t>((1u << CM) - 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cid = blockIdx.x / CM;
-  const int nclusters = gridDim.x / CM;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CM);  // one commit from each CTA of the pair
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0u;
-    mbar_fence_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if constexpr (CM > 1) cluster_sync();  // the peer's barriers exist before any multicast
-  const uint32_t tmem_base = *tmem_slot;
-
-  const WaitCtx wc{abort_flag, p.err, p.wait_ns};
-  const int num_pm = (p.num_m_tiles + CM - 1) / CM;  // M-tile pairs (the last may be half
-  const int num_super = num_pm * p.num_n_tiles;        // phantom: its loads read fill values)
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- producer
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;
-      bool skip_once = p.fault_inject != 0 && cid == 0 && rank == 0;
-      for (int st = cid; st < num_super; st += nclusters) {
-        int mp, nt;
-        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
-        const int mt = mp * CM + rank;
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          if (skip_once) {
-            skip_once = false;  // fault injection: this stage is never armed
-          } else {
-            const uint32_t fb = full0 + 8 * stage;
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            issue_stage<K, CM>(&tmA, &tmB, sA0 + stage * kAStage, sB0 + stage * kBStage, fb, mt,
-                               nt, kb, rank, p);
-            armed |= 1u << stage;
-            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          }
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-      }
-      // Every copy this thread issued must land before the CTA exits.
-      for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) wait_drain(full0 + 8 * s, (armed_par >> s) & 1u, wc);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, KindOf<K>::a_mn, KindOf<K>::b_mn);
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      for (int st = cid; st < num_super; st += nclusters, ++it) {
-        const int buf = it & 1;
-        const uint32_t acc_par = (it >> 1) & 1;
-        if (!wait_bounded(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + buf * kBN;
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = sA0 + stage * kAStage;
-          const uint32_t sb = sB0 + stage * kBStage;
-          // K-major: 16 K elements = 32 bytes further along the row; MN-major: 16 K rows
-          // of 128 bytes further down the chunk.
-          constexpr uint32_t kKSw = kKRowBytes == 128 ? 2u : 4u;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = KindOf<K>::a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
-                                                : sdesc(sa + kk * 32, 16, 8 * kKRowBytes, kKSw);
-            const uint64_t bd = KindOf<K>::b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
-                                                : sdesc(sb + kk * 32, 16, 8 * kKRowBytes, kKSw);
-            umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          if constexpr (CM > 1) umma_commit_mc(empty0 + 8 * stage, kPairMask);
-          else umma_commit(empty0 + 8 * stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(tfull0 + 8 * buf);
-      }
-      // Drain: every MMA issued above has completed once this commit arrives.
-      umma_commit(drain);
-      wait_drain(drain, 0, wc);
-    }
-  } else {
-    // ------------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    int it = 0;
-    for (int st = cid; st < num_super; st += nclusters, ++it) {
-      const int buf = it & 1;
-      const uint32_t acc_par = (it >> 1) & 1;
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(tfull0 + 8 * buf, acc_par, wc, kSiteEpiAccFull) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      __syncwarp();
-      tc_fence_after();
-      int mp, nt;
-      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
-      epilogue_tile<K>(tacc, row, mp * CM + rank, nt, p);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  // Neither CTA of a pair leaves while the other may still multicast into its shared
-  // memory or arrive on its barriers.
-  if constexpr (CM > 1) cluster_sync();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// ======================================================================================
-// CTA-pair kernel.  The two CTAs of a cluster run one tcgen05.mma.cta_group::2 stream:
-// M = 256 (each CTA's 128 A rows and 128 TMEM lanes), N = 256 (each CTA's shared memory
-// holds one 128-row half of B), so every B byte in shared memory feeds both SMs' tensor
-// cores.  Per SM and per 64-deep k-block that is 32 KB written by TMA and 32 KB read by the
-// tensor core, against 48 + 48 KB for one CTA computing a 128 x 256 tile alone (which
-// caps a single CTA near two thirds of the tensor rate on 128 B/clock of shared memory).
-// The 7-stage ring is 224 KB.
-//   warp 0 (both CTAs)  TMA producer for this CTA's A rows and B half, on its own barrier;
-//   warp 1 (even CTA)   allocates TMEM with its peer and issues the pair's MMAs;
-//   warp 1 (odd CTA)    allocates TMEM with its peer and relays "stage s has landed here"
-//                       to the even CTA (a remote mbarrier arrive);
-//   warps 2..5          epilogue of this CTA's 128 rows, releasing the accumulator to the
-//                       even CTA's MMA issuer.
-// ======================================================================================
+// One stage of one CTA of the pair: its own 128 A rows, and its 128-row half of B (K-major:
+// one box; MN-major: two 64-wide chunks).
 template <GemmKind K>
 __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CUtensorMap* tB,
                                                  uint32_t sa, uint32_t sb, uint32_t bar, int mt,

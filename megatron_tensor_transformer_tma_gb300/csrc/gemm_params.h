@@ -19,23 +19,15 @@ enum class GemmKind : int {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 64;     // k-block depth: 64 bf16 = 128-byte K-major rows
-constexpr int kStages = 4;  // 4 x 48 KB ring (32-deep blocks in 8 stages measured slower)
-constexpr int kAStage = kBM * kBK * 2;  // 16 KB
-constexpr int kBStage = kBN * kBK * 2;  // 32 KB
-constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kBK = 64;  // k-block depth: 64 bf16 = 128-byte K-major rows (128-byte swizzle;
+                         // 32-deep blocks with a 64-byte swizzle measured much slower)
 constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x kBK(K) MN-major box, 8 KB
-// K-major tiles use the swizzle whose row is one k-block (64 B for kBK = 32), MN-major
-// tiles the 128-byte swizzle (rows of 64 M/N elements).
-constexpr int kKRowBytes = kBK * 2;
-static_assert(kKRowBytes == 64 || kKRowBytes == 128, "K-major rows must be 64 or 128 bytes");
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kGemmSmem = kStages * kStageBytes + 1024 + 256;
-constexpr int kClusterM = 2;  // CTAs per cluster (a pair along M)
+constexpr int kClusterM = 2;  // CTAs per cluster: the pair along M
 
-// CTA-pair (cta_group::2) variant: a pair computes a 256 x 256 tile; each CTA keeps its
-// 128 rows of A and its 128-row half of B per stage, so a stage is 32 KB per CTA.
+// A pair computes a 256 x 256 tile; each CTA keeps its 128 rows of A and its 128-row half
+// of B per stage, so a stage is 32 KB per CTA.
 constexpr int kPairStages = 7;
 constexpr int kPairAStage = kBM * kBK * 2;         // 16 KB
 constexpr int kPairBStage = (kBN / 2) * kBK * 2;   // 16 KB
