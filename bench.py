@@ -164,6 +164,23 @@ def run_reference(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------------ multi-rank helpers
+def reduce_max(x: float, device, world: int) -> float:
+    """The maximum of x over all ranks (the job's step time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step (weak scaling)."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -321,13 +338,9 @@ def run_native(args, rank, world, local_rank):
     recs = mlpb.mlpb_read_timings(h, capacity=64 * kernel_steps)
     mlpb.mlpb_enable_timing(h, False)
     kernel_step_launches = sum(r["kernels"] for r in recs) / kernel_steps
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ms_total, dev, world)
     ms_step = ms_total / args.steps
-    flops_step = shape.gemm_flops()
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    value = job_tflops(shape.gemm_flops(), world, ms_step)
 
     # ---- per-kernel aggregation (CUDA events around each launch, same stream)
     per = {}
@@ -453,13 +466,8 @@ def run_e2e(args, shape, d, step, new_outputs, results, out0, dev, world):
     run(n)
     e1.record(comp)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": shape.gemm_flops() * world / (ms * 1e-3) / 1e12, "unit": UNIT,
+    ms = reduce_max(e0.elapsed_time(e1) / n, dev, world)
+    return {"value": job_tflops(shape.gemm_flops(), world, ms), "unit": UNIT,
             "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "api": "mlpb_forward + mlpb_backward (+ SP-LN) via the ctypes binding",
             "overlap": "H2D and D2H on their own streams, double-buffered device tensors"}
