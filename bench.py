@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--grad-accum", action="store_true",
+                   help="accumulate parameter gradients into fp32 main-grad buffers")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     return p.parse_args()
@@ -73,34 +75,42 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def config_of(shape, wid):
+def config_of(shape, wid, grad_accum=False):
     return {"workload": shape.name or f"workload {wid}", "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
             "activation": shape.act, "bias": shape.bias, "sp_layernorm": shape.sp_ln,
+            "grad_accum": bool(grad_accum),
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_step_fn(shape, wid, tokens):
-    """One fwd+bwd of the fp64 oracle on the first `tokens` rows of the workload."""
-    import numpy as np  # noqa: F401
+def oracle_step_fn(shape, wid, tokens, grad_accum=False):
+    """One fwd+bwd of the fp64 oracle on the first `tokens` rows of the workload (adding
+    the parameter gradients into carried main-grad buffers with `grad_accum`)."""
+    import numpy as np
     from inputs import make_inputs
     from oracle import layernorm as oln
     from oracle import mlp as omlp
     small = shape.with_tokens(tokens)
     d = make_inputs(small, wid)
     f = {k: (v.double().numpy() if v is not None else None) for k, v in d.items()}
+    main = {}
 
     def step():
         if shape.sp_ln:
             oln.block_forward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
                               f["W2"], f["b2"], shape.act, shape.tp)
-            oln.block_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
-                               f["W2"], f["dY"], shape.act, shape.tp)
+            g = oln.block_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"],
+                                   f["b1"], f["W2"], f["dY"], shape.act, shape.tp)
         else:
             omlp.mlp_forward(f["X"], f["W1"], f["b1"], f["W2"], f["b2"], shape.act)
-            omlp.mlp_backward(f["X"], f["W1"], f["b1"], f["W2"], f["dY"], shape.act)
+            g = omlp.mlp_backward(f["X"], f["W1"], f["b1"], f["W2"], f["dY"], shape.act)
+        if grad_accum:
+            if not main:
+                main.update({k: np.zeros(np.shape(v)) for k, v in g.items()
+                             if k in omlp.PARAM_GRADS and v is not None})
+            main.update(omlp.accumulate_param_grads(main, g))
     return step, small.gemm_flops()
 
 
@@ -111,17 +121,17 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(shape, wid, target_s):
+def cpu_baseline(shape, wid, target_s, grad_accum=False):
     """The oracle as it stands, timed on this host's cores on a bounded token sample."""
     tokens = 128
-    step, flops = oracle_step_fn(shape, wid, tokens)
+    step, flops = oracle_step_fn(shape, wid, tokens, grad_accum)
     t0 = time.perf_counter()
     step()
     dt = time.perf_counter() - t0
     reps = max(1, int(target_s / max(dt, 1e-3)))
     if reps > 4 and shape.tokens >= 1024:  # prefer one larger sample to many small ones
         tokens = min(shape.tokens, 128 * min(8, reps // 2))
-        step, flops = oracle_step_fn(shape, wid, tokens)
+        step, flops = oracle_step_fn(shape, wid, tokens, grad_accum)
         t0 = time.perf_counter()
         step()
         dt = time.perf_counter() - t0
@@ -145,7 +155,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     shape = bench_shape(args)
-    step, flops = oracle_step_fn(shape, args.workload, 128)
+    step, flops = oracle_step_fn(shape, args.workload, 128, args.grad_accum)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -156,7 +166,7 @@ def run_reference(args, rank, world):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": config_of(shape, args.workload),
+           "data": "synthetic", "config": config_of(shape, args.workload, args.grad_accum),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                             "sample": f"each step: fwd+bwd of the fp64 oracle on the first 128 "
                                       f"of {shape.tokens} tokens"},
@@ -258,12 +268,15 @@ def run_native(args, rank, world, local_rank):
     # the oracle baseline runs first, before any GPU work, on rank 0 at N = 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(shape, args.workload, args.cpu_seconds)
+        cpu = cpu_baseline(shape, args.workload, args.cpu_seconds, args.grad_accum)
 
     d = make_inputs(shape, args.workload)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     blk = mlpb.MLPBlock(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act, shape.bias,
-                        shape.sp_ln, shape.ln_eps)
+                        shape.sp_ln, shape.ln_eps,
+                        mlpb.MLPB_FLAG_ACCUMULATE_GRADS if args.grad_accum else 0)
+    # parameter-gradient buffers start at zero when they are accumulated into
+    new_param = torch.zeros if args.grad_accum else torch.empty
     T, H = shape.tokens, shape.hidden
     h = blk.handle
 
@@ -276,8 +289,8 @@ def run_native(args, rank, world, local_rank):
             o["mean"] = torch.empty((T,), dtype=torch.float32, device=dev)
             o["rstd"] = torch.empty((T,), dtype=torch.float32, device=dev)
             o["dX_ln"] = torch.empty((T, H), dtype=torch.float32, device=dev)
-            o["dgamma"] = torch.empty((H,), dtype=torch.float32, device=dev)
-            o["dbeta"] = torch.empty((H,), dtype=torch.float32, device=dev)
+            o["dgamma"] = new_param((H,), dtype=torch.float32, device=dev)
+            o["dbeta"] = new_param((H,), dtype=torch.float32, device=dev)
         return o
 
     def results(o):
@@ -384,7 +397,7 @@ def run_native(args, rank, world, local_rank):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
-               "config": config_of(shape, args.workload),
+               "config": config_of(shape, args.workload, args.grad_accum),
                "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
                "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
                "roofline": roofline, "kernels": kernels,

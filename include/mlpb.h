@@ -38,11 +38,13 @@
  *       Y, dX               [T][H] fp32
  *       dW1, dW2            fp32 in the layouts of W1, W2;  db1 [F], db2 [H] fp32
  *     where T = tokens, H = hidden, F = ffn, t = tp, Fs = F / t.
- *   - With T = 0 the activation pointers (X, Y, Z/A saved, dY, dX, workspace) may be
- *     NULL; the forward does nothing and the backward writes zero weight/bias grads.
+ *   - With T = 0 the per-row pointers (X, Y, Z/A saved, dY, dX, Xn, mean, rstd, dXn,
+ *     workspace) may be NULL; forwards do nothing and backwards write zero parameter
+ *     grads (weights, biases, gamma, beta), or leave them as they are when accumulating.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  Argument errors are returned synchronously and launch
- *     nothing.  Outputs are overwritten, never accumulated into.
+ *     nothing.  Outputs are overwritten, except the parameter gradients of a handle
+ *     created with MLPB_FLAG_ACCUMULATE_GRADS, which are added into.
  *   - A device-side bounded wait that expires (about one second) is recorded in
  *     a per-handle error word and reported by mlpb_last_device_error().
  *   - A handle may be used from one host thread at a time, and its calls must not
@@ -78,6 +80,15 @@ typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
 #define MLPB_FLAG_FAULT_INJECT 0x1u    /* test only: the first GEMM launch of the  \
                                           next forward skips one producer arrive, so \
                                           its consumers' bounded wait expires        */
+/* Gradient-accumulation fusion ("The Tensor-Parallel Primitives": the linear layers'
+ * shared autograd function accumulates weight gradients).  With this flag the parameter
+ * gradients of mlpb_backward (dW1, dW2, db1, db2) and mlpb_layernorm_sp_bwd (dgamma,
+ * dbeta) are ADDED to what their fp32 buffers hold (main-grad buffers carried across
+ * micro-batches) instead of overwriting them; the weight-gradient GEMM epilogues read,
+ * add and write each fp32 element once, the bias/LN parameter reductions add their final
+ * sums.  The caller zeroes the buffers before the first micro-batch.  With T = 0 the
+ * buffers are left as they are.  dX (an activation gradient) is always overwritten. */
+#define MLPB_FLAG_ACCUMULATE_GRADS 0x2u
 
 typedef struct {
   int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */

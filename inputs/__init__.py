@@ -10,6 +10,7 @@ from .mlp_inputs import (  # noqa: F401
     workload,
     make_inputs,
     make_ln_grad,
+    make_main_grads,
     sample_rows,
     sample_ffn_cols,
     reduced_tokens,

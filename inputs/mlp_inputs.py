@@ -26,7 +26,7 @@ SEED_BASE = 20261202
 
 # tensor index k in the per-tensor seed ``SEED_BASE + 1000*workload + k``
 _K = {"X": 0, "W1": 1, "b1": 2, "W2": 3, "b2": 4, "dY": 5, "gamma": 6,
-      "beta": 7, "dXn": 8, "rows": 9, "cols": 10}
+      "beta": 7, "dXn": 8, "rows": 9, "cols": 10, "main": 11}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -117,6 +117,18 @@ def make_ln_grad(shape: MLPShape, wid: int) -> torch.Tensor:
     """A seeded fp32 upstream gradient for a stand-alone LayerNorm backward."""
     g = _gen(wid, "dXn")
     return torch.randn((shape.tokens, shape.hidden), generator=g, dtype=torch.float32)
+
+
+def make_main_grads(shapes: dict, wid: int, scales: dict | None = None) -> dict:
+    """Seeded fp32 starting contents of main-grad buffers (the state a gradient-
+    accumulating backward adds into): one standard-normal tensor per name, in sorted
+    name order from one generator, times ``scales[name]`` (default 1)."""
+    g = _gen(wid, "main")
+    out = {}
+    for k in sorted(shapes):
+        x = torch.randn(shapes[k], generator=g, dtype=torch.float32)
+        out[k] = x.mul_(float((scales or {}).get(k, 1.0)))
+    return out
 
 
 def reduced_tokens(shape: MLPShape, tokens: int = 512) -> MLPShape:

@@ -87,6 +87,7 @@ struct mlpb_handle {
   int max_clusters;  // co-resident GEMM clusters
   uint32_t* d_err;  // device error word
   bool fault_pending;
+  bool accumulate;  // MLPB_FLAG_ACCUMULATE_GRADS: parameter gradients add into their outputs
   uint64_t wait_ns;
   // bias-grad split plans
   int db2_splits, db1_splits;
@@ -217,7 +218,7 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   if (c.act != MLPB_ACT_GELU_TANH && c.act != MLPB_ACT_SWIGLU) return MLPB_EINVAL;
   if (c.has_bias != 0 && c.has_bias != 1) return MLPB_EINVAL;
   if (c.seq_parallel_ln != 0 && c.seq_parallel_ln != 1) return MLPB_EINVAL;
-  if ((c.flags & ~MLPB_FLAG_FAULT_INJECT) != 0) return MLPB_EINVAL;
+  if ((c.flags & ~(MLPB_FLAG_FAULT_INJECT | MLPB_FLAG_ACCUMULATE_GRADS)) != 0) return MLPB_EINVAL;
   if (c.seq_parallel_ln && !(c.ln_eps > 0.f)) return MLPB_EINVAL;
   if (c.tokens % 128 != 0 || c.hidden % 64 != 0) return MLPB_EUNSUPPORTED;
   if (c.ffn % c.tp != 0 || (c.ffn / c.tp) % 8 != 0) return MLPB_EUNSUPPORTED;
@@ -239,6 +240,7 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   h->swiglu = c.act == MLPB_ACT_SWIGLU;
   h->F1 = f1;
   h->fault_pending = (c.flags & MLPB_FLAG_FAULT_INJECT) != 0;
+  h->accumulate = (c.flags & MLPB_FLAG_ACCUMULATE_GRADS) != 0;
   h->wait_ns = 1000000000ull;
   h->timing = false;
   h->d_err = nullptr;
@@ -409,7 +411,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
   mlpb_status st = MLPB_OK;
 
-  if (T == 0) {  // empty batch: every parameter gradient is zero
+  const int acc = h->accumulate ? 1 : 0;
+  if (T == 0) {  // empty batch: every parameter gradient is zero (adds nothing when accumulating)
+    if (acc) return MLPB_OK;
     st = from_cuda(launch_fill_zero(dW1, static_cast<size_t>(F1 * H * 4), s));
     if (st == MLPB_OK) st = from_cuda(launch_fill_zero(dW2, static_cast<size_t>(F * H * 4), s));
     if (st == MLPB_OK && bias) st = from_cuda(launch_fill_zero(db1, static_cast<size_t>(F * 4), s));
@@ -434,8 +438,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * H, 2);
-    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s2);
+    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H, 2);
+    cudaError_t e =
+        launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -449,6 +454,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW2;
+    p.accumulate = acc;
     const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
@@ -457,7 +463,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
       st = MLPB_EINVAL;
     else
       st = run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
-                    2.0 * (T * H + T * F) + 4.0 * H * F);
+                    2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
 
   // ---- [s] dgrad of fc2 with the fused activation derivative: dZ [T][F1]
@@ -487,8 +493,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- [s2] db1 = sum_t dZ
   if (st == MLPB_OK && bias) {
-    LaunchTimer lt(h, s2, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * F, 2);
-    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s2);
+    LaunchTimer lt(h, s2, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
+    cudaError_t e =
+        launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -501,11 +508,12 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
+    p.accumulate = acc;
     if (!map2d(&ta, dZ, F1, T, F1, 64, kBK) || !map2d(&tb, X, H, T, H, 64, kBK))
       st = MLPB_EINVAL;
     else
       st = run_gemm(h, GemmKind::WGRAD_W1, false, ta, tb, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
-                    2.0 * (T * F1 + T * H) + 4.0 * F1 * H);
+                    2.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
   }
 
   // ---- [s] dX = sum_i dZ_i W1_i  (f backward: the sum over shards is the K loop)
@@ -533,12 +541,14 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle* h, const void* X, const void* gamma,
                                   const void* beta, void* Xn, float* mean, float* rstd,
                                   mlpb_stream_t stream) {
-  if (h == nullptr || !X || !gamma || !beta || !Xn || !mean || !rstd) return MLPB_EINVAL;
+  if (h == nullptr || !gamma || !beta) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !Xn || !mean || !rstd)) return MLPB_EINVAL;  // T = 0: empty rows
   if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
   for (const void* p : {X, gamma, beta, static_cast<const void*>(Xn)})
-    if (!aligned16(p)) return MLPB_EINVAL;
+    if (p && !aligned16(p)) return MLPB_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t T = h->T, H = h->H;
+  if (T == 0) return MLPB_OK;
   LaunchTimer lt(h, s, "ln_fwd", 0.0, 4.0 * T * H + 8.0 * T + 4.0 * H);
   cudaError_t e = launch_ln_fwd(X, gamma, beta, Xn, mean, rstd, T, H, h->cfg.ln_eps,
                                 h->num_sms, h->d_err, h->wait_ns, s);
@@ -550,20 +560,22 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
                                   const float* mean, const float* rstd, const float* dXn,
                                   float* dX, float* dgamma, float* dbeta, void* workspace,
                                   mlpb_stream_t stream) {
-  if (h == nullptr || !X || !gamma || !mean || !rstd || !dXn || !dX || !dgamma || !dbeta ||
-      !workspace)
-    return MLPB_EINVAL;
+  if (h == nullptr || !gamma || !dgamma || !dbeta) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !mean || !rstd || !dXn || !dX || !workspace))
+    return MLPB_EINVAL;  // T = 0: the row tensors are empty
   if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
   for (const void* p : {X, gamma, static_cast<const void*>(dXn), static_cast<const void*>(dX),
                         static_cast<const void*>(workspace)})
-    if (!aligned16(p)) return MLPB_EINVAL;
+    if (p && !aligned16(p)) return MLPB_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t T = h->T, H = h->H;
   const int nblk = h->t * h->ln_blocks_per_shard;
   float* pg = static_cast<float*>(workspace);
   float* pb = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                        align256(static_cast<size_t>(nblk) * H * 4));
-  if (T == 0) {
+  const int acc = h->accumulate ? 1 : 0;
+  if (T == 0) {  // no rows: zero parameter gradients (adds nothing when accumulating)
+    if (acc) return MLPB_OK;
     cudaError_t e = launch_fill_zero(dgamma, static_cast<size_t>(H * 4), s);
     if (e == cudaSuccess) e = launch_fill_zero(dbeta, static_cast<size_t>(H * 4), s);
     return from_cuda(e);
@@ -573,8 +585,8 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
                                 h->ln_blocks_per_shard, h->d_err, h->wait_ns, s);
   lt.done();
   if (e == cudaSuccess) {
-    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * H, 1);
-    e = launch_sum_partials2(pg, pb, nblk, H, dgamma, dbeta, s);
+    LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * (1 + acc) * H, 1);
+    e = launch_sum_partials2(pg, pb, nblk, H, dgamma, dbeta, s, acc);
     lt2.done();
   }
   return from_cuda(e);

@@ -115,6 +115,20 @@ __device__ __forceinline__ void store_f32x32(float* p, int nvalid, const float (
   }
 }
 
+// v += the nvalid (a multiple of 4) fp32 values at p (read-modify-write accumulation).
+__device__ __forceinline__ void add_f32x32(const float* p, int nvalid, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (q * 4 < nvalid) {
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(p + q * 4));
+      v[q * 4 + 0] += o.x;
+      v[q * 4 + 1] += o.y;
+      v[q * 4 + 2] += o.z;
+      v[q * 4 + 3] += o.w;
+    }
+  }
+}
+
 __device__ __forceinline__ void tmem_load_f32x32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
@@ -252,7 +266,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       if (jc >= p.Fs) break;
       float v[32];
       tmem_load_f32x32(tacc + c * 32, v);
-      if (row_ok) store_f32x32(dW + jc, min(32, p.Fs - jc), v);
+      if (row_ok) {
+        const int nv = min(32, p.Fs - jc);
+        if (p.accumulate) add_f32x32(dW + jc, nv, v);
+        store_f32x32(dW + jc, nv, v);
+      }
     }
   } else {  // WGRAD_W1
     const int n0 = nt * kBN;
@@ -263,7 +281,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       if (col >= p.H) break;
       float v[32];
       tmem_load_f32x32(tacc + c * 32, v);
-      if (row_ok) store_f32x32(dW + col, min(32, p.H - col), v);
+      if (row_ok) {
+        const int nv = min(32, p.H - col);
+        if (p.accumulate) add_f32x32(dW + col, nv, v);
+        store_f32x32(dW + col, nv, v);
+      }
     }
   }
 }

@@ -47,6 +47,7 @@ struct GemmParams {
   uint32_t* err;
   uint64_t wait_ns;
   int fault_inject;
+  int accumulate;  // weight-gradient kinds: add into the fp32 output instead of overwriting
 };
 
 }  // namespace mlpb

@@ -20,14 +20,16 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
                             const GemmParams& p, int clusters, cudaStream_t s);
 
 // reduce.cu: column sums of a [R][C] bf16 matrix into fp32, deterministic two passes.
-//   pass 1: part[split][C] over row splits of `rows_per_split` rows; pass 2: out[C].
+//   pass 1: part[split][C] over row splits of `rows_per_split` rows; pass 2: out[C]
+//   (added to the existing out[C] when `accumulate`).
 cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
-                               int64_t rows_per_split, float* part, float* out, cudaStream_t s);
+                               int64_t rows_per_split, float* part, float* out, cudaStream_t s,
+                               int accumulate = 0);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
-                                cudaStream_t s);
+                                cudaStream_t s, int accumulate = 0);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
-                                 float* out_a, float* out_b, cudaStream_t s);
+                                 float* out_a, float* out_b, cudaStream_t s, int accumulate = 0);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 
 // layernorm.cu: rows streamed through a shared-memory ring by TMA bulk copies; bounded

@@ -72,13 +72,14 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
-// out[c] = sum_k part[k][c] for one or two partial arrays (blockIdx.y picks the array).
+// out[c] = sum_k part[k][c] (or out[c] += ... with `accumulate`) for one or two partial
+// arrays (blockIdx.y picks the array).
 // A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
 // eight warp sums are added in warp order -- a fixed order, so results are reproducible.
 __global__ void __launch_bounds__(256) sum_partials_kernel(const float* part_a,
                                                            const float* part_b, int nparts,
                                                            int64_t C, float* out_a,
-                                                           float* out_b) {
+                                                           float* out_b, int accumulate) {
   __shared__ float red[8][33];
   const float* part = blockIdx.y == 0 ? part_a : part_b;
   float* out = blockIdx.y == 0 ? out_a : out_b;
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(256) sum_partials_kernel(const float* part_a,
     float t = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) t += red[w][lane];
-    out[c] = t;
+    out[c] = accumulate ? out[c] + t : t;
   }
 }
 
@@ -107,27 +108,28 @@ __global__ void fill_zero_kernel(uint4* p, size_t n16, uint8_t* tail, size_t nta
 }
 
 cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
-                               int64_t rows_per_split, float* part, float* out, cudaStream_t s) {
+                               int64_t rows_per_split, float* part, float* out, cudaStream_t s,
+                               int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + kColsPerCta - 1) / kColsPerCta),
                   static_cast<unsigned>(splits));
   colsum_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), R, C,
                                            rows_per_split, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_sum_partials(part, splits, C, out, s);
+  return launch_sum_partials(part, splits, C, out, s, accumulate);
 }
 
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
-                                cudaStream_t s) {
+                                cudaStream_t s, int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 1);
-  sum_partials_kernel<<<grid, 256, 0, s>>>(part, part, nparts, C, out, out);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part, part, nparts, C, out, out, accumulate);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
-                                 float* out_a, float* out_b, cudaStream_t s) {
+                                 float* out_a, float* out_b, cudaStream_t s, int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 2);
-  sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, part_b, nparts, C, out_a, out_b);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, part_b, nparts, C, out_a, out_b, accumulate);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ MLPB_ENOMEM = -5
 MLPB_ACT_GELU_TANH = 0
 MLPB_ACT_SWIGLU = 1
 MLPB_FLAG_FAULT_INJECT = 0x1
+MLPB_FLAG_ACCUMULATE_GRADS = 0x2
 
 # Every symbol include/mlpb.h declares.
 EXPORTED = (
@@ -291,14 +292,18 @@ class MLPBlock:
         return Y
 
     def alloc_grads(self, W1, W2):
+        """dX plus the parameter-gradient buffers; zeroed main-grad buffers when the handle
+        accumulates (MLPB_FLAG_ACCUMULATE_GRADS)."""
         c = self.cfg
         has_b = bool(c.has_bias)
+        new = torch.zeros if c.flags & MLPB_FLAG_ACCUMULATE_GRADS else torch.empty
+        f32 = dict(dtype=torch.float32, device=self.device)
         return dict(
-            dX=torch.empty((c.tokens, c.hidden), dtype=torch.float32, device=self.device),
-            dW1=torch.empty(W1.shape, dtype=torch.float32, device=self.device),
-            dW2=torch.empty(W2.shape, dtype=torch.float32, device=self.device),
-            db1=torch.empty((c.ffn,), dtype=torch.float32, device=self.device) if has_b else None,
-            db2=torch.empty((c.hidden,), dtype=torch.float32, device=self.device) if has_b else None,
+            dX=torch.empty((c.tokens, c.hidden), **f32),
+            dW1=new(W1.shape, **f32),
+            dW2=new(W2.shape, **f32),
+            db1=new((c.ffn,), **f32) if has_b else None,
+            db2=new((c.hidden,), **f32) if has_b else None,
         )
 
     def backward(self, X, W1, W2, dY, grads=None, stream=None):

@@ -209,6 +209,27 @@ def mlp_backward(X, W1, b1, W2, dY, act="gelu", store=None):
     return {"dX": dX, "dW1": dW1, "dW2": shard_w2_grad(dW2f, t), "db1": db1, "db2": db2}
 
 
+# ---------------------------------------------------------------- gradient accumulation
+PARAM_GRADS = ("dW1", "dW2", "db1", "db2", "dgamma", "dbeta")
+
+
+def accumulate_param_grads(main, grads):
+    """One micro-batch of gradient accumulation ([Tour] §Tensor-Parallel Primitives:
+    the linear layers' autograd function accumulates the weight gradients).
+
+    ``main`` holds the main-grad buffers carried across micro-batches; the result is
+    main[k] + grads[k] for every parameter gradient (``PARAM_GRADS``) present in both.
+    Activation gradients (dX, dXn) are per micro-batch and are not accumulated.
+    Reading: the step's loss is the sum of the micro-batches' losses, so its parameter
+    gradient is the plain sum of theirs (no averaging by the micro-batch count).
+    """
+    out = {}
+    for k in PARAM_GRADS:
+        if main.get(k) is not None and grads.get(k) is not None:
+            out[k] = _f64(main[k]) + _f64(grads[k])
+    return out
+
+
 # ---------------------------------------------------------------- explicitly sharded path
 def mlp_forward_sharded(X, W1, b1, W2, b2, act="gelu"):
     """Forward as t tensor-parallel ranks would run it, each with its own buffers.

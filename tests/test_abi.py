@@ -60,6 +60,29 @@ def test_create_rejects_bad_configs(lib, kw, status):
     assert not h.value
 
 
+def test_accumulate_flag_passes_config_validation(lib):
+    """Without a GPU, a valid config fails only at the device query (ECUDA), so a flag
+    that validation accepts shows as not-EINVAL and an unknown one as EINVAL."""
+    for flags, ok in ((mlpb.MLPB_FLAG_ACCUMULATE_GRADS, True),
+                      (mlpb.MLPB_FLAG_ACCUMULATE_GRADS | mlpb.MLPB_FLAG_FAULT_INJECT, True),
+                      (0x4, False)):
+        cfg = mlpb.make_config(128, 256, 1024, 2, "gelu", True, flags=flags)
+        h = ctypes.c_void_p()
+        st = lib.mlpb_create(ctypes.byref(cfg), ctypes.byref(h))
+        if ok:
+            assert st != mlpb.MLPB_EINVAL
+            lib.mlpb_destroy(h)
+        else:
+            assert st == mlpb.MLPB_EINVAL and not h.value
+
+
+def test_header_flag_values_match_binding():
+    src = open(os.path.join(ROOT, "include", "mlpb.h")).read()
+    for name in ("MLPB_FLAG_FAULT_INJECT", "MLPB_FLAG_ACCUMULATE_GRADS"):
+        m = re.search(rf"#define\s+{name}\s+(0x[0-9a-fA-F]+)u", src)
+        assert m and int(m.group(1), 16) == getattr(mlpb, name), name
+
+
 def test_null_arguments(lib):
     h = ctypes.c_void_p()
     assert lib.mlpb_create(None, ctypes.byref(h)) == mlpb.MLPB_EINVAL

@@ -23,6 +23,14 @@ def _free_port():
 
 
 def _worker(rank, world, port, q):
+    try:
+        q.put((rank, _run(rank, world, port)))
+    except Exception as e:  # reported to the parent at once instead of a queue timeout
+        q.put((rank, {"error": repr(e)}))
+        raise
+
+
+def _run(rank, world, port):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -30,24 +38,27 @@ def _worker(rank, world, port, q):
     import torch
     out = {"max": bench.reduce_max(1.5 + rank, torch.device("cpu"), world)}
     out["tflops"] = bench.job_tflops(2e12, world, 10.0)
-    args = type("A", (), dict(workload=1, tp=None, tokens=None, warmup=0, steps=1))()
+    args = type("A", (), dict(workload=1, tp=None, tokens=None, warmup=0, steps=1,
+                              grad_accum=False))()
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.run_reference(args, rank, world)
     out["printed"] = buf.getvalue()
     dist.barrier()
     dist.destroy_process_group()
-    q.put((rank, out))
+    return out
 
 
 def test_two_gloo_ranks():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q), daemon=True) for r in range(2)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=300) for _ in procs)
+    for r in range(2):
+        assert "error" not in res[r], f"rank {r}: {res[r].get('error')}"
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0

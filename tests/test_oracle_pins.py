@@ -205,6 +205,55 @@ def test_backward_is_linear_in_dY():
         assert _rel(c[k], a[k] + b[k]) < 1e-12
 
 
+# ------------------------------------------------------------------ gradient accumulation
+def _split_tokens(a, parts):
+    return np.split(np.asarray(a), parts, axis=0)
+
+
+@pytest.mark.parametrize("act,bias", [("gelu", True), ("swiglu", False)])
+def test_accumulated_micro_batches_equal_concatenated_batch(act, bias):
+    """The gradient of a loss summed over tokens is the sum over any split of the tokens:
+    accumulating three micro-batches from zeroed buffers gives the whole batch's
+    parameter gradients (the batch backward is a separate computation, not a sum)."""
+    d = _mlp_inputs(12, 16, 32, 2, act, bias, seed=21)
+    full = mlp.mlp_backward(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], act)
+    main = {k: np.zeros_like(full[k]) for k in mlp.PARAM_GRADS if full.get(k) is not None}
+    for Xk, dYk in zip(_split_tokens(d["X"], 3), _split_tokens(d["dY"], 3)):
+        g = mlp.mlp_backward(Xk, d["W1"], d["b1"], d["W2"], dYk, act)
+        main = mlp.accumulate_param_grads(main, g)
+    assert set(main) == ({"dW1", "dW2", "db1", "db2"} if bias else {"dW1", "dW2", "db2"})
+    for k, v in main.items():
+        assert _rel(v, full[k]) < 1e-12, k
+
+
+def test_accumulation_adds_to_existing_main_grads_and_skips_dX():
+    d = _mlp_inputs(8, 16, 32, 2, "gelu", True, seed=22)
+    g = mlp.mlp_backward(d["X"], d["W1"], d["b1"], d["W2"], d["dY"], "gelu")
+    r = np.random.default_rng(23)
+    main0 = {k: r.standard_normal(np.shape(g[k])) for k in ("dW1", "dW2", "db1", "db2")}
+    main0["dX"] = r.standard_normal(g["dX"].shape)
+    out = mlp.accumulate_param_grads(main0, g)
+    assert "dX" not in out
+    for k in ("dW1", "dW2", "db1", "db2"):
+        assert np.array_equal(out[k], main0[k] + g[k]), k
+    # an all-zero micro-batch (T = 0 has no tokens) leaves the buffers as they are
+    z = mlp.accumulate_param_grads(main0, {k: np.zeros_like(main0[k]) for k in main0})
+    for k in ("dW1", "dW2", "db1", "db2"):
+        assert np.array_equal(z[k], main0[k]), k
+
+
+def test_accumulated_layernorm_params_equal_concatenated_batch():
+    X, gamma, beta, _ = _ln_inputs(8, 16, 24)
+    d = _mlp_inputs(8, 16, 32, 2, "swiglu", False, seed=25)
+    full = ln.block_backward(X, gamma, beta, 1e-5, d["W1"], None, d["W2"], d["dY"], "swiglu", 2)
+    main = {"dgamma": np.zeros(16), "dbeta": np.zeros(16), "dW1": np.zeros_like(full["dW1"])}
+    for Xk, dYk in zip(_split_tokens(X, 2), _split_tokens(d["dY"], 2)):
+        g = ln.block_backward(Xk, gamma, beta, 1e-5, d["W1"], None, d["W2"], dYk, "swiglu", 2)
+        main = mlp.accumulate_param_grads(main, g)
+    for k in ("dgamma", "dbeta", "dW1"):
+        assert _rel(main[k], full[k]) < 1e-12, k
+
+
 # ------------------------------------------------------------------ LayerNorm
 def _ln_inputs(T, H, seed):
     r = np.random.default_rng(seed)
@@ -359,6 +408,8 @@ def _all_pins_pass():
         test_layernorm_backward_rowsum_zero_and_fd()
         test_sp_block_equals_plain_composition("swiglu")
         test_layernorm_unit_gamma_invariants()
+        test_accumulated_micro_batches_equal_concatenated_batch("gelu", True)
+        test_accumulation_adds_to_existing_main_grads_and_skips_dX()
     except AssertionError:
         return False
     return True
@@ -386,7 +437,19 @@ def _mut_layernorm_bwd(X, gamma, mean, rstd, dXn):
     return dX, (dXn * xhat).sum(axis=0), dXn.sum(axis=0)
 
 
+def _mut_accumulate_overwrites(main, grads):
+    return {k: np.asarray(grads[k], dtype=np.float64) for k in mlp.PARAM_GRADS
+            if main.get(k) is not None and grads.get(k) is not None}
+
+
+def _mut_accumulate_averages(main, grads):
+    return {k: 0.5 * (np.asarray(main[k]) + np.asarray(grads[k])) for k in mlp.PARAM_GRADS
+            if main.get(k) is not None and grads.get(k) is not None}
+
+
 @pytest.mark.parametrize("target,attr,mutant", [
+    (mlp, "accumulate_param_grads", _mut_accumulate_overwrites),
+    (mlp, "accumulate_param_grads", _mut_accumulate_averages),
     (mlp, "gelu_tanh", _mut_dropped_cubic),
     (mlp, "silu_grad", _mut_silu_grad),
     (mlp, "full_w2", _mut_full_w2),
