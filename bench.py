@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--branch", action="store_true",
+                   help="the pre-norm MLP branch with its residual (SP-LN workloads)")
     p.add_argument("--grad-accum", action="store_true",
                    help="accumulate parameter gradients into fp32 main-grad buffers")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -75,17 +77,18 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def config_of(shape, wid, grad_accum=False):
-    return {"workload": shape.name or f"workload {wid}", "tokens": shape.tokens,
+def config_of(shape, wid, grad_accum=False, branch=False):
+    return {"workload": (shape.name or f"workload {wid}") + (" + residual" if branch else ""),
+            "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
             "activation": shape.act, "bias": shape.bias, "sp_layernorm": shape.sp_ln,
-            "grad_accum": bool(grad_accum),
+            "residual_branch": bool(branch), "grad_accum": bool(grad_accum),
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_step_fn(shape, wid, tokens, grad_accum=False):
+def oracle_step_fn(shape, wid, tokens, grad_accum=False, branch=False):
     """One fwd+bwd of the fp64 oracle on the first `tokens` rows of the workload (adding
     the parameter gradients into carried main-grad buffers with `grad_accum`)."""
     import numpy as np
@@ -98,7 +101,12 @@ def oracle_step_fn(shape, wid, tokens, grad_accum=False):
     main = {}
 
     def step():
-        if shape.sp_ln:
+        if branch:
+            oln.branch_forward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
+                               f["W2"], f["b2"], shape.act, shape.tp)
+            g = oln.branch_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"],
+                                    f["b1"], f["W2"], f["dY"], shape.act, shape.tp)
+        elif shape.sp_ln:
             oln.block_forward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
                               f["W2"], f["b2"], shape.act, shape.tp)
             g = oln.block_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"],
@@ -121,17 +129,17 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(shape, wid, target_s, grad_accum=False):
+def cpu_baseline(shape, wid, target_s, grad_accum=False, branch=False):
     """The oracle as it stands, timed on this host's cores on a bounded token sample."""
     tokens = 128
-    step, flops = oracle_step_fn(shape, wid, tokens, grad_accum)
+    step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch)
     t0 = time.perf_counter()
     step()
     dt = time.perf_counter() - t0
     reps = max(1, int(target_s / max(dt, 1e-3)))
     if reps > 4 and shape.tokens >= 1024:  # prefer one larger sample to many small ones
         tokens = min(shape.tokens, 128 * min(8, reps // 2))
-        step, flops = oracle_step_fn(shape, wid, tokens, grad_accum)
+        step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch)
         t0 = time.perf_counter()
         step()
         dt = time.perf_counter() - t0
@@ -148,6 +156,8 @@ def cpu_baseline(shape, wid, target_s, grad_accum=False):
 def bench_shape(args):
     from inputs import workload
     shape = workload(args.workload, args.tp)
+    if getattr(args, "branch", False) and not shape.sp_ln:
+        raise SystemExit("--branch needs a workload with the sequence-parallel LayerNorm")
     return shape if args.tokens is None else shape.with_tokens(args.tokens)
 
 
@@ -155,7 +165,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     shape = bench_shape(args)
-    step, flops = oracle_step_fn(shape, args.workload, 128, args.grad_accum)
+    step, flops = oracle_step_fn(shape, args.workload, 128, args.grad_accum, args.branch)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -166,7 +176,8 @@ def run_reference(args, rank, world):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": config_of(shape, args.workload, args.grad_accum),
+           "data": "synthetic",
+           "config": config_of(shape, args.workload, args.grad_accum, args.branch),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                             "sample": f"each step: fwd+bwd of the fp64 oracle on the first 128 "
                                       f"of {shape.tokens} tokens"},
@@ -268,13 +279,18 @@ def run_native(args, rank, world, local_rank):
     # the oracle baseline runs first, before any GPU work, on rank 0 at N = 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(shape, args.workload, args.cpu_seconds, args.grad_accum)
+        cpu = cpu_baseline(shape, args.workload, args.cpu_seconds, args.grad_accum,
+                           args.branch)
 
     d = make_inputs(shape, args.workload)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
-    blk = mlpb.MLPBlock(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act, shape.bias,
-                        shape.sp_ln, shape.ln_eps,
-                        mlpb.MLPB_FLAG_ACCUMULATE_GRADS if args.grad_accum else 0)
+    flags = mlpb.MLPB_FLAG_ACCUMULATE_GRADS if args.grad_accum else 0
+    if args.branch:
+        blk = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
+                             shape.bias, shape.ln_eps, flags)
+    else:
+        blk = mlpb.MLPBlock(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
+                            shape.bias, shape.sp_ln, shape.ln_eps, flags)
     # parameter-gradient buffers start at zero when they are accumulated into
     new_param = torch.zeros if args.grad_accum else torch.empty
     T, H = shape.tokens, shape.hidden
@@ -284,7 +300,7 @@ def run_native(args, rank, world, local_rank):
         """Device buffers of one step's results (and the LN intermediates it needs)."""
         o = {"Y": torch.empty((T, H), dtype=torch.float32, device=dev)}
         o.update(blk.alloc_grads(g["W1"], g["W2"]))
-        if shape.sp_ln:
+        if shape.sp_ln and not args.branch:
             o["Xn"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
             o["mean"] = torch.empty((T,), dtype=torch.float32, device=dev)
             o["rstd"] = torch.empty((T,), dtype=torch.float32, device=dev)
@@ -295,7 +311,9 @@ def run_native(args, rank, world, local_rank):
 
     def results(o):
         """The step's results a caller reads back (intermediates excluded)."""
-        if shape.sp_ln:
+        if args.branch:
+            keys = ["Y", "dX", "dW1", "dW2", "dgamma", "dbeta"]
+        elif shape.sp_ln:
             keys = ["Y", "dX_ln", "dW1", "dW2", "dgamma", "dbeta"]
         else:
             keys = ["Y", "dX", "dW1", "dW2"] + (["db1", "db2"] if shape.bias else [])
@@ -304,6 +322,11 @@ def run_native(args, rank, world, local_rank):
     out = new_outputs()
 
     def step(src, o=out):
+        if args.branch:  # Y = X + MLP(LN(X)) and its backward, two calls
+            blk.forward(src["X"], src["gamma"], src["beta"], src["W1"], src["b1"], src["W2"],
+                        src["b2"], o["Y"])
+            blk.backward(src["X"], src["gamma"], src["W1"], src["W2"], src["dY"], o)
+            return
         X = src["X"]
         if shape.sp_ln:
             mlpb.mlpb_layernorm_sp_fwd(h, X, src["gamma"], src["beta"], o["Xn"], o["mean"],
@@ -397,7 +420,7 @@ def run_native(args, rank, world, local_rank):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
-               "config": config_of(shape, args.workload, args.grad_accum),
+               "config": config_of(shape, args.workload, args.grad_accum, args.branch),
                "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
                "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
                "roofline": roofline, "kernels": kernels,

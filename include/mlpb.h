@@ -172,6 +172,34 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle *h, const void *X, const void *gam
                                   float *dX, float *dgamma, float *dbeta, void *workspace,
                                   mlpb_stream_t stream);
 
+/* Pre-norm MLP branch of a transformer layer ("The Transformer Stack": the layer runs
+ * its MLP branch on the layer-normalised input and adds the branch input back through a
+ * residual connection; dropout is left out), sequence-parallel:
+ *     Y = X + MLP(LN(X))        (Y [T][H] fp32; X, gamma, beta bf16)
+ * Runs mlpb_layernorm_sp_fwd (writes Xn, mean, rstd, kept for the backward) and the
+ * forward of mlpb_forward on Xn, with X added to every output element in fc2's epilogue
+ * after b2 (the residual of a row lives on the sequence shard that owns the row).
+ * Requires seq_parallel_ln.  Arguments as in the two calls it combines. */
+mlpb_status mlpb_branch_forward(mlpb_handle *h, const void *X, const void *gamma,
+                                const void *beta, const void *W1, const void *b1,
+                                const void *W2, const void *b2, float *Y, void *Xn,
+                                float *mean, float *rstd, void *Zsaved, void *Asaved,
+                                void *workspace, mlpb_stream_t stream);
+
+/* Backward of mlpb_branch_forward for an upstream gradient dY [T][H] bf16:
+ *     dX = dY + LN'(dXn),  dXn = the MLP backward's input gradient on Xn
+ * plus dW1, dW2, db1, db2 (as mlpb_backward, on Xn) and dgamma, dbeta (as
+ * mlpb_layernorm_sp_bwd).  dXn is formed in the dX buffer and the LayerNorm backward
+ * rewrites it in place with the residual gradient dY added in its epilogue, so the call
+ * needs no [T][H] buffer beyond dX.  `workspace` holds mlpb_workspace_size() bytes.
+ * Honours MLPB_FLAG_ACCUMULATE_GRADS for the parameter gradients. */
+mlpb_status mlpb_branch_backward(mlpb_handle *h, const void *X, const void *gamma,
+                                 const void *W1, const void *W2, const void *Xn,
+                                 const float *mean, const float *rstd, const void *Zsaved,
+                                 const void *Asaved, const void *dY, float *dX, float *dW1,
+                                 float *dW2, float *db1, float *db2, float *dgamma,
+                                 float *dbeta, void *workspace, mlpb_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device error word.  Returns
  * MLPB_ETIMEOUT if a bounded wait expired since the last call, MLPB_ECUDA if
  * the stream reported an error, else MLPB_OK. */

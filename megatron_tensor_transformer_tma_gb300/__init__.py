@@ -1,4 +1,4 @@
 """GB300 (sm_103a) tensor-parallel transformer MLP block: a C-ABI CUDA library
 (libmlpb) and its thin ctypes binding."""
 from .mlpb import *  # noqa: F401,F403
-from .mlpb import MLPBlock, MLPBError, load_library  # noqa: F401
+from .mlpb import MLPBlock, MLPBError, MLPBranch, load_library  # noqa: F401

@@ -318,6 +318,14 @@ mlpb_status mlpb_saved_size(const mlpb_handle* h, size_t* z_bytes, size_t* a_byt
   return MLPB_OK;
 }
 
+static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                                const void* W2, const void* b2, float* Y, void* Zsaved,
+                                void* Asaved, const void* resid, cudaStream_t s);
+static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
+                               const float* mean, const float* rstd, const float* dXn,
+                               const void* dres, float* dX, float* dgamma, float* dbeta,
+                               void* workspace, cudaStream_t s);
+
 mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const void* b1,
                          const void* W2, const void* b2, float* Y, void* Zsaved, void* Asaved,
                          void* workspace, mlpb_stream_t stream) {
@@ -331,7 +339,16 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
                         static_cast<const void*>(Asaved), b1, b2})
     if (p && !aligned16(p)) return MLPB_EINVAL;
   if (h->T == 0) return MLPB_OK;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return forward_impl(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, nullptr,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+// fc1 and fc2 of a validated forward; `resid` (bf16 [T][H] or NULL) is added to Y in
+// fc2's epilogue after b2.
+static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                                const void* W2, const void* b2, float* Y, void* Zsaved,
+                                void* Asaved, const void* resid, cudaStream_t s) {
+  const bool bias = h->cfg.has_bias != 0;
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t;
 
   // ---- fc1 (column-parallel; f forward = every shard reads the same X)
@@ -385,9 +402,11 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
     q.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     q.num_kb = static_cast<int>(t * q.kb_per_shard);
     q.bias = static_cast<const __nv_bfloat16*>(b2);
+    q.aux = static_cast<const __nv_bfloat16*>(resid);
     q.out0 = Y;
     st = run_gemm(h, GemmKind::FC2, true, ta, tb, q, s, "fc2", 2.0 * T * H * F,
-                  2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0));
+                  2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
+                      (resid ? 2.0 * T * H : 0.0));
   }
   return st;
 }
@@ -567,7 +586,15 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
   for (const void* p : {X, gamma, static_cast<const void*>(dXn), static_cast<const void*>(dX),
                         static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return MLPB_EINVAL;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return ln_bwd_impl(h, X, gamma, mean, rstd, dXn, nullptr, dX, dgamma, dbeta, workspace,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+// LayerNorm backward of validated arguments; `dres` (bf16 [T][H] or NULL) is added to dX.
+static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
+                               const float* mean, const float* rstd, const float* dXn,
+                               const void* dres, float* dX, float* dgamma, float* dbeta,
+                               void* workspace, cudaStream_t s) {
   const int64_t T = h->T, H = h->H;
   const int nblk = h->t * h->ln_blocks_per_shard;
   float* pg = static_cast<float*>(workspace);
@@ -580,8 +607,9 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
     if (e == cudaSuccess) e = launch_fill_zero(dbeta, static_cast<size_t>(H * 4), s);
     return from_cuda(e);
   }
-  LaunchTimer lt(h, s, "ln_bwd", 0.0, 10.0 * T * H + 8.0 * T + 10.0 * H);
-  cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dX, pg, pb, T, H, h->t,
+  LaunchTimer lt(h, s, "ln_bwd", 0.0,
+                 (dres ? 12.0 : 10.0) * T * H + 8.0 * T + 10.0 * H);
+  cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dres, dX, pg, pb, T, H, h->t,
                                 h->ln_blocks_per_shard, h->d_err, h->wait_ns, s);
   lt.done();
   if (e == cudaSuccess) {
@@ -590,6 +618,52 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
     lt2.done();
   }
   return from_cuda(e);
+}
+
+mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma,
+                                const void* beta, const void* W1, const void* b1,
+                                const void* W2, const void* b2, float* Y, void* Xn, float* mean,
+                                float* rstd, void* Zsaved, void* Asaved, void* workspace,
+                                mlpb_stream_t stream) {
+  if (h == nullptr) return MLPB_EINVAL;
+  const bool bias = h->cfg.has_bias != 0;
+  if (!gamma || !beta || !W1 || !W2) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !Xn || !mean || !rstd || !Y || !Zsaved || !Asaved)) return MLPB_EINVAL;
+  if (bias != (b1 != nullptr) || bias != (b2 != nullptr)) return MLPB_EINVAL;
+  if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
+  for (const void* p : {X, gamma, beta, static_cast<const void*>(Xn), W1, W2,
+                        static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
+                        static_cast<const void*>(Asaved), b1, b2})
+    if (p && !aligned16(p)) return MLPB_EINVAL;
+  (void)workspace;
+  if (h->T == 0) return MLPB_OK;
+  mlpb_status st = mlpb_layernorm_sp_fwd(h, X, gamma, beta, Xn, mean, rstd, stream);
+  if (st != MLPB_OK) return st;
+  return forward_impl(h, Xn, W1, b1, W2, b2, Y, Zsaved, Asaved, X,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+mlpb_status mlpb_branch_backward(mlpb_handle* h, const void* X, const void* gamma,
+                                 const void* W1, const void* W2, const void* Xn,
+                                 const float* mean, const float* rstd, const void* Zsaved,
+                                 const void* Asaved, const void* dY, float* dX, float* dW1,
+                                 float* dW2, float* db1, float* db2, float* dgamma, float* dbeta,
+                                 void* workspace, mlpb_stream_t stream) {
+  if (h == nullptr) return MLPB_EINVAL;
+  if (!h->cfg.seq_parallel_ln) return MLPB_EUNSUPPORTED;
+  if (!gamma || !dgamma || !dbeta) return MLPB_EINVAL;
+  if (h->T > 0 && (!X || !Xn || !mean || !rstd)) return MLPB_EINVAL;
+  for (const void* p : {X, gamma})
+    if (p && !aligned16(p)) return MLPB_EINVAL;
+  // The MLP backward on the normalised input writes dXn into dX; the LayerNorm backward
+  // then rewrites dX in place, row by row, as dY + LN'(dXn).  The parameter reductions of
+  // both steps share the workspace one after the other (the first step's side stream has
+  // joined the caller's stream when mlpb_backward returns).
+  mlpb_status st = mlpb_backward(h, Xn, W1, W2, Zsaved, Asaved, dY, dX, dW1, dW2, db1, db2,
+                                 workspace, stream);
+  if (st != MLPB_OK) return st;
+  return ln_bwd_impl(h, X, gamma, mean, rstd, dX, dY, dX, dgamma, dbeta, workspace,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 mlpb_status mlpb_last_device_error(mlpb_handle* h, mlpb_stream_t stream) {

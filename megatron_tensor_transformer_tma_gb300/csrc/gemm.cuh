@@ -21,7 +21,7 @@
 //   FC1_GELU      Z = X W1^T + b1, A = gelu(Z)       M=T  N=F      K=H   A,B K-major
 //   FC1_SWIGLU    [G|U] = X [Wg_i|Wu_i]^T, A = silu(G)U  (per shard i, 128 gate + 128 up
 //                 columns per tile: the even CTA holds the gate rows, the odd the up rows)
-//   FC2           Y = sum_i A_i W2_i^T + b2           M=T  N=H      K=t x Fs (walks shards)
+//   FC2           Y = sum_i A_i W2_i^T + b2 (+ R)     M=T  N=H      K=t x Fs (walks shards)
 //   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B MN-major
 //   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B MN-major
 //   DX            dX = sum_i dZ_i W1_i                M=T  N=H      K=F1  B MN-major
@@ -205,6 +205,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         load_bf16x32(p.bias + col, nv, b);
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] += b[e];
+      }
+      if (K == GemmKind::FC2 && p.aux != nullptr && row_ok) {  // residual, added after b2
+        float r[32];
+        load_bf16x32(p.aux + static_cast<size_t>(m) * p.H + col, nv, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += r[e];
       }
       if (row_ok) store_f32x32(Y + col, nv, v);
     }

@@ -41,7 +41,7 @@ struct GemmParams {
   int M;                // valid output rows
   int T, H, F, Fs, t;
   const __nv_bfloat16* bias;  // FC1_GELU: b1; FC2: b2 (nullable)
-  const __nv_bfloat16* aux;   // DGRAD_*: saved Z or G|U
+  const __nv_bfloat16* aux;   // DGRAD_*: saved Z or G|U;  FC2: residual R [T][H] or NULL
   void* out0;
   void* out1;
   uint32_t* err;

@@ -37,9 +37,11 @@ cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Xn,
                           float* mean, float* rstd, int64_t T, int64_t H, float eps, int num_sms,
                           uint32_t* err, uint64_t wait_ns, cudaStream_t s);
+// dres (bf16 [T][H], or NULL) is added to dX: the gradient of a residual around the
+// normalised branch.  dXn may equal dX (in place, row by row).
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
-                          const float* dXn, float* dX, float* part_dg, float* part_db,
-                          int64_t T, int64_t H, int shards, int blocks_per_shard, uint32_t* err,
-                          uint64_t wait_ns, cudaStream_t s);
+                          const float* dXn, const void* dres, float* dX, float* part_dg,
+                          float* part_db, int64_t T, int64_t H, int shards, int blocks_per_shard,
+                          uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace mlpb

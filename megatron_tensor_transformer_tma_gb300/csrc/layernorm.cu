@@ -186,11 +186,15 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
 }
 
 // ------------------------------------------------------------------ backward
-template <int kVpt>
+// With kRes, dX also receives the residual branch's gradient dres (bf16 [T][H]):
+// dX = dres + LN'(dXn).  dXn and dX may be the same buffer: each row of dXn is copied
+// whole into shared memory (and waited for) before any element of that row of dX is
+// written, and no other CTA touches the row.
+template <int kVpt, bool kRes>
 __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
-    const float* __restrict__ mean, const float* __restrict__ rstd,
-    const float* __restrict__ dXn, float* __restrict__ dX, float* __restrict__ part_dg,
+    const float* __restrict__ mean, const float* __restrict__ rstd, const float* dXn,
+    const __nv_bfloat16* __restrict__ dres, float* dX, float* __restrict__ part_dg,
     float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnBwdThreads;
@@ -273,7 +277,16 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     block_sum<NT, 2>(s, sh);
     const float mg = s[0] / static_cast<float>(H);
     const float mgx = s[1] / static_cast<float>(H);
-    // pass 2: dx, and this CTA's dgamma / dbeta partials
+    // pass 2: dx, and this CTA's dgamma / dbeta partials.  The residual gradient's row
+    // is fetched first, all of this thread's vectors at once, ahead of the stores.
+    uint4 rpk[kRes ? kVpt : 1];
+    if constexpr (kRes) {
+#pragma unroll
+      for (int k = 0; k < kVpt; ++k) {
+        const int vi = threadIdx.x + k * NT;
+        rpk[k] = vi * 8 < H ? ld_global_nc_v4(dres + row * H + vi * 8) : make_uint4(0, 0, 0, 0);
+      }
+    }
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int vi = threadIdx.x + k * NT;
@@ -287,6 +300,12 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
         o[e] = rs * (dy[e] * gm[e] - mg - xh * mgx);
         adg[k][e] += dy[e] * xh;
         adb[k][e] += dy[e];
+      }
+      if constexpr (kRes) {
+        float r[8];
+        bf16x8_to_f32(rpk[k], r);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(o[e], r[e]);  // a plain add, never an FMA
       }
       st_f32x8(dX + row * H + vi * 8, o);
     }
@@ -362,32 +381,41 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
 }
 
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
-                          const float* dXn, float* dX, float* part_dg, float* part_db,
-                          int64_t T, int64_t H, int shards, int blocks_per_shard, uint32_t* err,
-                          uint64_t wait_ns, cudaStream_t s) {
+                          const float* dXn, const void* dres, float* dX, float* part_dg,
+                          float* part_db, int64_t T, int64_t H, int shards, int blocks_per_shard,
+                          uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
   const size_t row = static_cast<size_t>(H) * 6;
   const int nbuf = 2;  // two 256-thread CTAs per SM, each with a two-row ring
   const size_t smem = nbuf * row + 8 * nbuf;
   const unsigned grid = static_cast<unsigned>(shards * blocks_per_shard);
   const auto* x = static_cast<const __nv_bfloat16*>(X);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
+  const auto* r = static_cast<const __nv_bfloat16*>(dres);
   const int Hi = static_cast<int>(H);
   const int64_t rps = T / shards;
   cudaError_t e = cudaSuccess;
   switch (ln_vpt(H, kLnBwdThreads)) {
-#define MLPB_LN_BWD(V)                                                                          \
-  case V:                                                                                       \
-    e = set_smem(ln_bwd_kernel<V>, smem);                                                       \
-    if (e == cudaSuccess)                                                                       \
-      ln_bwd_kernel<V><<<grid, kLnBwdThreads, smem, s>>>(x, g, mean, rstd, dXn, dX, part_dg,    \
-                                                         part_db, rps, blocks_per_shard, Hi,    \
-                                                         nbuf, err, wait_ns);                   \
+#define MLPB_LN_BWD_RES(V, R)                                                                \
+  e = set_smem(ln_bwd_kernel<V, R>, smem);                                                   \
+  if (e == cudaSuccess)                                                                      \
+    ln_bwd_kernel<V, R><<<grid, kLnBwdThreads, smem, s>>>(x, g, mean, rstd, dXn, r, dX,      \
+                                                          part_dg, part_db, rps,             \
+                                                          blocks_per_shard, Hi, nbuf, err,   \
+                                                          wait_ns);
+#define MLPB_LN_BWD(V)          \
+  case V:                       \
+    if (r != nullptr) {         \
+      MLPB_LN_BWD_RES(V, true)  \
+    } else {                    \
+      MLPB_LN_BWD_RES(V, false) \
+    }                           \
     break;
     MLPB_LN_BWD(1)
     MLPB_LN_BWD(2)
     MLPB_LN_BWD(4)
     MLPB_LN_BWD(8)
 #undef MLPB_LN_BWD
+#undef MLPB_LN_BWD_RES
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -33,6 +33,7 @@ EXPORTED = (
     "mlpb_create", "mlpb_destroy", "mlpb_workspace_size", "mlpb_saved_size", "mlpb_forward",
     "mlpb_backward", "mlpb_layernorm_sp_fwd", "mlpb_layernorm_sp_bwd", "mlpb_last_device_error",
     "mlpb_enable_timing", "mlpb_read_timings", "mlpb_status_str", "mlpb_bias_grad_noalloc",
+    "mlpb_branch_forward", "mlpb_branch_backward",
 )
 
 
@@ -83,6 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mlpb_read_timings": (I, [H, ctypes.POINTER(mlpb_kernel_time), I, ctypes.POINTER(I)]),
         "mlpb_status_str": (ctypes.c_char_p, [I]),
         "mlpb_bias_grad_noalloc": (I, [P, ctypes.c_int64, ctypes.c_int64, P, P]),
+        "mlpb_branch_forward": (I, [H] + [P] * 15),
+        "mlpb_branch_backward": (I, [H] + [P] * 19),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -227,6 +230,45 @@ def mlpb_layernorm_sp_bwd(h: Handle, X, gamma, mean, rstd, dXn, dX, dgamma, dbet
            "mlpb_layernorm_sp_bwd")
 
 
+def mlpb_branch_forward(h: Handle, X, gamma, beta, W1, b1, W2, b2, Y, Xn, mean, rstd, Zsaved,
+                        Asaved, workspace=None, stream=None):
+    c = h.cfg
+    T, Hd, F, t = c.tokens, c.hidden, c.ffn, c.tp
+    bf, f32 = torch.bfloat16, torch.float32
+    f1 = 2 * F if c.act == MLPB_ACT_SWIGLU else F
+    args = [
+        _ptr(X, bf, (T, Hd), "X"), _ptr(gamma, bf, (Hd,), "gamma"), _ptr(beta, bf, (Hd,), "beta"),
+        _ptr(W1, bf, _w1_shape(c), "W1"), _ptr(b1, bf, (F,), "b1"),
+        _ptr(W2, bf, (t, Hd, F // t), "W2"), _ptr(b2, bf, (Hd,), "b2"),
+        _ptr(Y, f32, (T, Hd), "Y"), _ptr(Xn, bf, (T, Hd), "Xn"), _ptr(mean, f32, (T,), "mean"),
+        _ptr(rstd, f32, (T,), "rstd"), _ptr(Zsaved, bf, (T, f1), "Zsaved"),
+        _ptr(Asaved, bf, (T, F), "Asaved"), _ptr(workspace, None, None, "workspace"),
+    ]
+    _check(load_library().mlpb_branch_forward(h.ptr, *args, _stream(stream)),
+           "mlpb_branch_forward")
+
+
+def mlpb_branch_backward(h: Handle, X, gamma, W1, W2, Xn, mean, rstd, Zsaved, Asaved, dY, dX,
+                         dW1, dW2, db1, db2, dgamma, dbeta, workspace, stream=None):
+    c = h.cfg
+    T, Hd, F, t = c.tokens, c.hidden, c.ffn, c.tp
+    bf, f32 = torch.bfloat16, torch.float32
+    f1 = 2 * F if c.act == MLPB_ACT_SWIGLU else F
+    args = [
+        _ptr(X, bf, (T, Hd), "X"), _ptr(gamma, bf, (Hd,), "gamma"),
+        _ptr(W1, bf, _w1_shape(c), "W1"), _ptr(W2, bf, (t, Hd, F // t), "W2"),
+        _ptr(Xn, bf, (T, Hd), "Xn"), _ptr(mean, f32, (T,), "mean"), _ptr(rstd, f32, (T,), "rstd"),
+        _ptr(Zsaved, bf, (T, f1), "Zsaved"), _ptr(Asaved, bf, (T, F), "Asaved"),
+        _ptr(dY, bf, (T, Hd), "dY"), _ptr(dX, f32, (T, Hd), "dX"),
+        _ptr(dW1, f32, _w1_shape(c), "dW1"), _ptr(dW2, f32, (t, Hd, F // t), "dW2"),
+        _ptr(db1, f32, (F,), "db1"), _ptr(db2, f32, (Hd,), "db2"),
+        _ptr(dgamma, f32, (Hd,), "dgamma"), _ptr(dbeta, f32, (Hd,), "dbeta"),
+        _ptr(workspace, None, None, "workspace"),
+    ]
+    _check(load_library().mlpb_branch_backward(h.ptr, *args, _stream(stream)),
+           "mlpb_branch_backward")
+
+
 def mlpb_last_device_error(h: Handle, stream=None) -> int:
     """Returns the status code (MLPB_OK, MLPB_ETIMEOUT, MLPB_ECUDA) without raising."""
     return load_library().mlpb_last_device_error(h.ptr, _stream(stream))
@@ -310,4 +352,38 @@ class MLPBlock:
         g = grads if grads is not None else self.alloc_grads(W1, W2)
         mlpb_backward(self.handle, X, W1, W2, self.Z, self.A, dY, g["dX"], g["dW1"], g["dW2"],
                       g["db1"], g["db2"], self.workspace, stream)
+        return g
+
+
+class MLPBranch(MLPBlock):
+    """The sequence-parallel pre-norm MLP branch Y = X + MLP(LN(X)) of one shape: an
+    MLPBlock whose handle has the LayerNorm enabled, plus the saved Xn, mean and rstd."""
+
+    def __init__(self, tokens, hidden, ffn, tp, act="gelu", has_bias=True, ln_eps=1e-5,
+                 flags=0, device="cuda"):
+        super().__init__(tokens, hidden, ffn, tp, act, has_bias, True, ln_eps, flags, device)
+        self.Xn = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=self.device)
+        self.mean = torch.empty((tokens,), dtype=torch.float32, device=self.device)
+        self.rstd = torch.empty((tokens,), dtype=torch.float32, device=self.device)
+
+    def forward(self, X, gamma, beta, W1, b1, W2, b2, Y=None, stream=None):
+        if Y is None:
+            Y = torch.empty((self.cfg.tokens, self.cfg.hidden), dtype=torch.float32,
+                            device=self.device)
+        mlpb_branch_forward(self.handle, X, gamma, beta, W1, b1, W2, b2, Y, self.Xn, self.mean,
+                            self.rstd, self.Z, self.A, self.workspace, stream)
+        return Y
+
+    def alloc_grads(self, W1, W2):
+        g = super().alloc_grads(W1, W2)
+        new = torch.zeros if self.cfg.flags & MLPB_FLAG_ACCUMULATE_GRADS else torch.empty
+        g["dgamma"] = new((self.cfg.hidden,), dtype=torch.float32, device=self.device)
+        g["dbeta"] = new((self.cfg.hidden,), dtype=torch.float32, device=self.device)
+        return g
+
+    def backward(self, X, gamma, W1, W2, dY, grads=None, stream=None):
+        g = grads if grads is not None else self.alloc_grads(W1, W2)
+        mlpb_branch_backward(self.handle, X, gamma, W1, W2, self.Xn, self.mean, self.rstd, self.Z,
+                             self.A, dY, g["dX"], g["dW1"], g["dW2"], g["db1"], g["db2"],
+                             g["dgamma"], g["dbeta"], self.workspace, stream)
         return g

@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the sequence-parallel LayerNorm and the pre-LN block.
+"""fp64 CPU oracle of the sequence-parallel LayerNorm, the pre-LN block and the
+pre-norm MLP branch with its residual connection.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / reference leg of ``bench.py`` may import this module.
@@ -168,6 +169,32 @@ def block_sp_forward_backward(X, gamma, beta, eps, W1, b1, W2, b2, dY, act, t):
         dgamma, dbeta = dgamma + dg, dbeta + db
     return {"Y": Y, "Xn": Xn, "dXn": dXn, "dX": dX, "dW1": dW1, "dW2": dW2,
             "dgamma": dgamma, "dbeta": dbeta}
+
+
+# ---------------------------------------------------------------- pre-norm MLP branch
+# [Tour] §The Transformer Stack: the layer runs its MLP branch on the layer-normalised
+# input and adds the branch input back through a residual connection.  Dropout is left
+# out (it is stochastic), so with the branch input X:
+#   out = X + MLP(LN(X)),   dX = dout + LN'(dXn)   (dXn: the MLP's input gradient)
+def branch_forward(X, gamma, beta, eps, W1, b1, W2, b2, act, t, store=None):
+    out = block_forward(X, gamma, beta, eps, W1, b1, W2, b2, act, t, store)
+    out["Y"] = _f64(X) + out["Y"]
+    return out
+
+
+def branch_backward(X, gamma, beta, eps, W1, b1, W2, dY, act, t, store=None):
+    g = block_backward(X, gamma, beta, eps, W1, b1, W2, dY, act, t, store)
+    g["dX"] = _f64(dY) + g["dX"]  # the residual path carries dout unchanged
+    return g
+
+
+def branch_rows(X, gamma, beta, eps, W1, b1, W2, b2, dY, rows, act, store=None):
+    """Y[rows] and dX[rows] of the pre-norm branch."""
+    rows = np.asarray(rows)
+    r = block_rows(X, gamma, beta, eps, W1, b1, W2, b2, dY, rows, act, store)
+    r["Y"] = _f64(X)[rows] + r["Y"]
+    r["dX"] = _f64(dY)[rows] + r["dX"]
+    return r
 
 
 def block_rows(X, gamma, beta, eps, W1, b1, W2, b2, dY, rows, act, store=None):

@@ -352,6 +352,61 @@ def test_block_backward_matches_finite_differences():
             assert abs((lp - lm) / (2 * h) - gflat[k]) < 1e-6 * max(1.0, abs(gflat[k]))
 
 
+# ------------------------------------------------------------------ pre-norm MLP branch
+@pytest.mark.parametrize("act,bias", [("gelu", True), ("swiglu", False)])
+def test_branch_backward_matches_finite_differences(act, bias):
+    """dX of out = X + MLP(LN(X)) against central differences of sum(dY * out); the
+    residual path makes dX differ from the block's by exactly the upstream gradient."""
+    t = 2
+    d = _mlp_inputs(6, 16, 16, t, act, bias, seed=61)
+    X, gamma, beta, _ = _ln_inputs(6, 16, 62)
+    eps = 1e-5
+    g = ln.branch_backward(X, gamma, beta, eps, d["W1"], d["b1"], d["W2"], d["dY"], act, t)
+
+    def loss():
+        y = ln.branch_forward(X, gamma, beta, eps, d["W1"], d["b1"], d["W2"], d["b2"], act,
+                              t)["Y"]
+        return float((d["dY"] * y).sum())
+
+    h = 1e-6
+    for arr, grad in ((X, g["dX"]), (gamma, g["dgamma"]), (beta, g["dbeta"]),
+                      (d["W2"], g["dW2"])):
+        flat, gflat = arr.reshape(-1), grad.reshape(-1)
+        for k in range(0, flat.size, max(1, flat.size // 8)):
+            old = flat[k]
+            flat[k] = old + h
+            lp = loss()
+            flat[k] = old - h
+            lm = loss()
+            flat[k] = old
+            assert abs((lp - lm) / (2 * h) - gflat[k]) < 1e-6 * max(1.0, abs(gflat[k]))
+
+
+def test_branch_with_zero_fc2_is_the_residual_alone():
+    """W2 = 0: the MLP adds only b2, so out = X + b2 exactly and dX = dY exactly (the
+    LayerNorm sees a zero gradient: dgamma = dbeta = 0)."""
+    d = _mlp_inputs(8, 16, 32, 2, "gelu", True, seed=63)
+    X, gamma, beta, _ = _ln_inputs(8, 16, 64)
+    W2 = np.zeros_like(d["W2"])
+    f = ln.branch_forward(X, gamma, beta, 1e-5, d["W1"], d["b1"], W2, d["b2"], "gelu", 2)
+    g = ln.branch_backward(X, gamma, beta, 1e-5, d["W1"], d["b1"], W2, d["dY"], "gelu", 2)
+    assert np.array_equal(f["Y"], X + d["b2"])
+    assert np.array_equal(g["dX"], d["dY"])
+    assert not g["dgamma"].any() and not g["dbeta"].any()
+
+
+def test_branch_rows_match_full():
+    d = _mlp_inputs(12, 16, 32, 2, "swiglu", False, seed=65)
+    X, gamma, beta, _ = _ln_inputs(12, 16, 66)
+    f = ln.branch_forward(X, gamma, beta, 1e-5, d["W1"], None, d["W2"], None, "swiglu", 2)
+    g = ln.branch_backward(X, gamma, beta, 1e-5, d["W1"], None, d["W2"], d["dY"], "swiglu", 2)
+    rows = [0, 5, 11]
+    r = ln.branch_rows(X, gamma, beta, 1e-5, d["W1"], None, d["W2"], None, d["dY"], rows,
+                       "swiglu")
+    assert _rel(r["Y"], f["Y"][rows]) < 1e-13
+    assert _rel(r["dX"], g["dX"][rows]) < 1e-13
+
+
 # ------------------------------------------------------------------ sampled modes
 @pytest.mark.parametrize("act,bias", [("gelu", True), ("swiglu", False)])
 def test_sampled_rows_and_cols_match_full(act, bias):
@@ -410,6 +465,8 @@ def _all_pins_pass():
         test_layernorm_unit_gamma_invariants()
         test_accumulated_micro_batches_equal_concatenated_batch("gelu", True)
         test_accumulation_adds_to_existing_main_grads_and_skips_dX()
+        test_branch_backward_matches_finite_differences("gelu", True)
+        test_branch_with_zero_fc2_is_the_residual_alone()
     except AssertionError:
         return False
     return True
@@ -447,7 +504,20 @@ def _mut_accumulate_averages(main, grads):
             if main.get(k) is not None and grads.get(k) is not None}
 
 
+def _mut_branch_backward_drops_residual(X, gamma, beta, eps, W1, b1, W2, dY, act, t,
+                                        store=None):
+    return ln.block_backward(X, gamma, beta, eps, W1, b1, W2, dY, act, t, store)
+
+
+def _mut_branch_forward_residual_sign(X, gamma, beta, eps, W1, b1, W2, b2, act, t, store=None):
+    out = ln.block_forward(X, gamma, beta, eps, W1, b1, W2, b2, act, t, store)
+    out["Y"] = out["Y"] - np.asarray(X, dtype=np.float64)
+    return out
+
+
 @pytest.mark.parametrize("target,attr,mutant", [
+    (ln, "branch_backward", _mut_branch_backward_drops_residual),
+    (ln, "branch_forward", _mut_branch_forward_residual_sign),
     (mlp, "accumulate_param_grads", _mut_accumulate_overwrites),
     (mlp, "accumulate_param_grads", _mut_accumulate_averages),
     (mlp, "gelu_tanh", _mut_dropped_cubic),
