@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
     bulk_load(buf0 + b * row_bytes, X + row * H, xbytes, bar0 + 8 * b);
     bulk_load(buf0 + b * row_bytes + xbytes, dXn + row * H, 4u * H, bar0 + 8 * b);
+    // the residual gradient's row is read with plain loads in pass 2; start it towards L2
+    if constexpr (kRes) bulk_prefetch_l2(dres + row * H, xbytes);
   };
   if (threadIdx.x == 0) {
     abort_flag = 0u;
