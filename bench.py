@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--branch", action="store_true",
                    help="the pre-norm MLP branch with its residual (SP-LN workloads)")
+    p.add_argument("--recompute", action="store_true",
+                   help="recompute the activation output in the backward (keep only Z)")
     p.add_argument("--grad-accum", action="store_true",
                    help="accumulate parameter gradients into fp32 main-grad buffers")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -77,12 +79,13 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def config_of(shape, wid, grad_accum=False, branch=False):
+def config_of(shape, wid, grad_accum=False, branch=False, recompute=False):
     return {"workload": (shape.name or f"workload {wid}") + (" + residual" if branch else ""),
             "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
             "activation": shape.act, "bias": shape.bias, "sp_layernorm": shape.sp_ln,
             "residual_branch": bool(branch), "grad_accum": bool(grad_accum),
+            "recompute_act": bool(recompute),
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
@@ -177,7 +180,8 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": config_of(shape, args.workload, args.grad_accum, args.branch),
+           "config": config_of(shape, args.workload, args.grad_accum, args.branch,
+                               args.recompute),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                             "sample": f"each step: fwd+bwd of the fp64 oracle on the first 128 "
                                       f"of {shape.tokens} tokens"},
@@ -285,6 +289,8 @@ def run_native(args, rank, world, local_rank):
     d = make_inputs(shape, args.workload)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     flags = mlpb.MLPB_FLAG_ACCUMULATE_GRADS if args.grad_accum else 0
+    if args.recompute:
+        flags |= mlpb.MLPB_FLAG_RECOMPUTE_ACT
     if args.branch:
         blk = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
                              shape.bias, shape.ln_eps, flags)
@@ -420,7 +426,8 @@ def run_native(args, rank, world, local_rank):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
-               "config": config_of(shape, args.workload, args.grad_accum, args.branch),
+               "config": config_of(shape, args.workload, args.grad_accum, args.branch,
+                               args.recompute),
                "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
                "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
                "roofline": roofline, "kernels": kernels,

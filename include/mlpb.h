@@ -89,6 +89,15 @@ typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
  * sums.  The caller zeroes the buffers before the first micro-batch.  With T = 0 the
  * buffers are left as they are.  dX (an activation gradient) is always overwritten. */
 #define MLPB_FLAG_ACCUMULATE_GRADS 0x2u
+/* Selective activation recomputation (the concept note's "Key math": activation
+ * recomputation, selective granularity).  With this flag mlpb_backward does not read
+ * the forward's A: the dgrad GEMM's epilogue, which already reads the saved Z (or G, U)
+ * for the activation derivative, also rewrites A = act(Z) into the Asaved buffer, and
+ * the dW2 GEMM runs after it on that A.  Only Z (G, U) must survive from the forward to
+ * the backward; the T*F bf16 A buffer can be scratch shared with other work (the
+ * forward writes it for fc2, the backward rewrites it).  A is recomputed from the
+ * bf16-rounded Z, so dW2 can differ from the stored-A path by bf16 rounding. */
+#define MLPB_FLAG_RECOMPUTE_ACT 0x4u
 
 typedef struct {
   int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */
@@ -147,9 +156,11 @@ mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const vo
  * shard; dW2_i = dY^T A_i; dW1_i = dZ_i^T X; db1 = sum_t dZ; db2 = sum_t dY;
  * dX = sum_i dZ_i W1_i with the sum over shards accumulated in one tensor-memory
  * accumulator (the emulated f all-reduce).  db1/db2 must be NULL without bias.
- * `workspace` must hold mlpb_workspace_size() bytes. */
+ * `workspace` must hold mlpb_workspace_size() bytes.  Asaved is read only (the
+ * forward's A), except under MLPB_FLAG_RECOMPUTE_ACT, where it is scratch that the
+ * backward writes before reading. */
 mlpb_status mlpb_backward(mlpb_handle *h, const void *X, const void *W1, const void *W2,
-                          const void *Zsaved, const void *Asaved, const void *dY,
+                          const void *Zsaved, void *Asaved, const void *dY,
                           float *dX, float *dW1, float *dW2, float *db1, float *db2,
                           void *workspace, mlpb_stream_t stream);
 
@@ -157,7 +168,8 @@ mlpb_status mlpb_backward(mlpb_handle *h, const void *X, const void *W1, const v
  * run on sequence-sharded activations).  Shard s owns rows [s*T/t, (s+1)*T/t);
  * each row r gets mean[r], rstd[r] = 1/sqrt(var + eps) (biased variance) and
  * Xn[r] = (X[r]-mean)*rstd*gamma + beta in bf16.  The emulated all-gather is
- * the row-block layout of Xn itself (or a copy kernel with EMULATE_COPIES).
+ * the row-block layout of Xn itself: shard s writes rows s*T/t.. of the gathered
+ * tensor that fc1 reads, so no copy is made.
  * X, gamma, beta bf16; mean, rstd [T] fp32.  Requires seq_parallel_ln. */
 mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle *h, const void *X, const void *gamma,
                                   const void *beta, void *Xn, float *mean, float *rstd,
@@ -196,7 +208,7 @@ mlpb_status mlpb_branch_forward(mlpb_handle *h, const void *X, const void *gamma
 mlpb_status mlpb_branch_backward(mlpb_handle *h, const void *X, const void *gamma,
                                  const void *W1, const void *W2, const void *Xn,
                                  const float *mean, const float *rstd, const void *Zsaved,
-                                 const void *Asaved, const void *dY, float *dX, float *dW1,
+                                 void *Asaved, const void *dY, float *dX, float *dW1,
                                  float *dW2, float *db1, float *db2, float *dgamma,
                                  float *dbeta, void *workspace, mlpb_stream_t stream);
 

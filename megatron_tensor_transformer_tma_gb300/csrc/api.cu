@@ -88,6 +88,7 @@ struct mlpb_handle {
   uint32_t* d_err;  // device error word
   bool fault_pending;
   bool accumulate;  // MLPB_FLAG_ACCUMULATE_GRADS: parameter gradients add into their outputs
+  bool recompute;   // MLPB_FLAG_RECOMPUTE_ACT: the backward rewrites A from the saved Z
   uint64_t wait_ns;
   // bias-grad split plans
   int db2_splits, db1_splits;
@@ -218,7 +219,9 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   if (c.act != MLPB_ACT_GELU_TANH && c.act != MLPB_ACT_SWIGLU) return MLPB_EINVAL;
   if (c.has_bias != 0 && c.has_bias != 1) return MLPB_EINVAL;
   if (c.seq_parallel_ln != 0 && c.seq_parallel_ln != 1) return MLPB_EINVAL;
-  if ((c.flags & ~(MLPB_FLAG_FAULT_INJECT | MLPB_FLAG_ACCUMULATE_GRADS)) != 0) return MLPB_EINVAL;
+  if ((c.flags & ~(MLPB_FLAG_FAULT_INJECT | MLPB_FLAG_ACCUMULATE_GRADS |
+                   MLPB_FLAG_RECOMPUTE_ACT)) != 0)
+    return MLPB_EINVAL;
   if (c.seq_parallel_ln && !(c.ln_eps > 0.f)) return MLPB_EINVAL;
   if (c.tokens % 128 != 0 || c.hidden % 64 != 0) return MLPB_EUNSUPPORTED;
   if (c.ffn % c.tp != 0 || (c.ffn / c.tp) % 8 != 0) return MLPB_EUNSUPPORTED;
@@ -241,6 +244,7 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   h->F1 = f1;
   h->fault_pending = (c.flags & MLPB_FLAG_FAULT_INJECT) != 0;
   h->accumulate = (c.flags & MLPB_FLAG_ACCUMULATE_GRADS) != 0;
+  h->recompute = (c.flags & MLPB_FLAG_RECOMPUTE_ACT) != 0;
   h->wait_ns = 1000000000ull;
   h->timing = false;
   h->d_err = nullptr;
@@ -412,7 +416,7 @@ static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, c
 }
 
 mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const void* W2,
-                          const void* Zsaved, const void* Asaved, const void* dY, float* dX,
+                          const void* Zsaved, void* Asaved, const void* dY, float* dX,
                           float* dW1, float* dW2, float* db1, float* db2, void* workspace,
                           mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;
@@ -421,8 +425,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   if (h->T > 0 && (!X || !Zsaved || !Asaved || !dY || !dX || !workspace))
     return MLPB_EINVAL;  // T = 0: the activation tensors are empty
   if (bias != (db1 != nullptr) || bias != (db2 != nullptr)) return MLPB_EINVAL;
-  for (const void* p : {X, W1, W2, Zsaved, Asaved, dY, static_cast<const void*>(dX),
-                        static_cast<const void*>(dW1), static_cast<const void*>(dW2),
+  for (const void* p : {X, W1, W2, Zsaved, static_cast<const void*>(Asaved), dY,
+                        static_cast<const void*>(dX), static_cast<const void*>(dW1),
+                        static_cast<const void*>(dW2),
                         static_cast<const void*>(db1), static_cast<const void*>(db2),
                         static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return MLPB_EINVAL;
@@ -464,8 +469,10 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     st = from_cuda(e);
   }
 
-  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
-  if (st == MLPB_OK) {
+  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T).  With recomputation A is
+  // rewritten by the dgrad epilogue below, so dW2 runs after it.
+  auto run_dw2 = [&]() -> mlpb_status {
+    CUtensorMap ta, tb;
     GemmParams p = base_params(h);
     p.M = static_cast<int>(H);
     p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
@@ -479,11 +486,12 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
     const uint32_t bbox[3] = {64, kBK, 1};
     if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
-      st = MLPB_EINVAL;
-    else
-      st = run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
+      return MLPB_EINVAL;
+    return run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
                     2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
-  }
+  };
+  const bool recompute = h->recompute;
+  if (st == MLPB_OK && !recompute) st = run_dw2();
 
   // ---- [s] dgrad of fc2 with the fused activation derivative: dZ [T][F1]
   if (st == MLPB_OK) {
@@ -495,6 +503,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_kb = static_cast<int>(cdiv(H, kBK));
     p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
     p.out0 = dZ;
+    p.out1 = recompute ? Asaved : nullptr;
     const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
@@ -504,11 +513,12 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     else
       st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, ta, tb,
                     p, s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H,
-                    2.0 * (T * H + F * H + 2 * T * F1));
+                    2.0 * (T * H + F * H + 2 * T * F1) + (recompute ? 2.0 * T * F : 0.0));
   }
   if (st == MLPB_OK && (cudaEventRecord(h->ev_dz, s) != cudaSuccess ||
                         cudaStreamWaitEvent(s2, h->ev_dz, 0) != cudaSuccess))
     st = MLPB_ECUDA;
+  if (st == MLPB_OK && recompute) st = run_dw2();
 
   // ---- [s2] db1 = sum_t dZ
   if (st == MLPB_OK && bias) {
@@ -646,7 +656,7 @@ mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma
 mlpb_status mlpb_branch_backward(mlpb_handle* h, const void* X, const void* gamma,
                                  const void* W1, const void* W2, const void* Xn,
                                  const float* mean, const float* rstd, const void* Zsaved,
-                                 const void* Asaved, const void* dY, float* dX, float* dW1,
+                                 void* Asaved, const void* dY, float* dX, float* dW1,
                                  float* dW2, float* db1, float* db2, float* dgamma, float* dbeta,
                                  void* workspace, mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;

@@ -24,6 +24,7 @@
 //   FC2           Y = sum_i A_i W2_i^T + b2 (+ R)     M=T  N=H      K=t x Fs (walks shards)
 //   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B MN-major
 //   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B MN-major
+//                 (both may also rewrite A = act(saved Z) for dW2: recomputation)
 //   DX            dX = sum_i dZ_i W1_i                M=T  N=H      K=F1  B MN-major
 //   WGRAD_W2      dW2_i = dY^T A_i                    M=H  N=F      K=T   A,B MN-major
 //   WGRAD_W1      dW1 = dZ^T X                        M=F1 N=H      K=T   A,B MN-major
@@ -220,6 +221,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const size_t base = static_cast<size_t>(m) * p.F + static_cast<size_t>(i) * p.Fs;
     const __nv_bfloat16* Z = p.aux + base;
     __nv_bfloat16* dZ = static_cast<__nv_bfloat16*>(p.out0) + base;
+    // recomputation: A = gelu(Z) from the saved Z, for the dW2 GEMM that follows
+    __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + base : nullptr;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       const int jc = j0 + c * 32;
@@ -229,6 +232,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int nv = min(32, p.Fs - jc);
       if (row_ok) {
         load_bf16x32(Z + jc, nv, z);
+        if (A != nullptr) {
+          float a[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = gelu_f(z[e]);
+          store_bf16x32(A + jc, nv, a);
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
         store_bf16x32(dZ + jc, nv, v);
@@ -240,6 +249,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const size_t base = static_cast<size_t>(m) * 2 * p.F + static_cast<size_t>(i) * 2 * p.Fs;
     const __nv_bfloat16* GU = p.aux + base;
     __nv_bfloat16* dGU = static_cast<__nv_bfloat16*>(p.out0) + base;
+    // recomputation: A = silu(G) U from the saved G, U, for the dW2 GEMM that follows
+    __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F +
+                                    static_cast<size_t>(i) * p.Fs
+                              : nullptr;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       const int jc = j0 + c * 32;
@@ -251,6 +264,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         float g[32], u[32];
         load_bf16x32(GU + jc, nv, g);
         load_bf16x32(GU + p.Fs + jc, nv, u);
+        if (A != nullptr) {
+          float a[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = u[e] * (g[e] * sigmoid_f(g[e]));
+          store_bf16x32(A + jc, nv, a);
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float s = sigmoid_f(g[e]);

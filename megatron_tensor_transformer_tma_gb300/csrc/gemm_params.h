@@ -43,7 +43,7 @@ struct GemmParams {
   const __nv_bfloat16* bias;  // FC1_GELU: b1; FC2: b2 (nullable)
   const __nv_bfloat16* aux;   // DGRAD_*: saved Z or G|U;  FC2: residual R [T][H] or NULL
   void* out0;
-  void* out1;
+  void* out1;  // FC1_*: A;  DGRAD_*: A recomputed from the saved Z, or NULL
   uint32_t* err;
   uint64_t wait_ns;
   int fault_inject;

@@ -27,6 +27,7 @@ MLPB_ACT_GELU_TANH = 0
 MLPB_ACT_SWIGLU = 1
 MLPB_FLAG_FAULT_INJECT = 0x1
 MLPB_FLAG_ACCUMULATE_GRADS = 0x2
+MLPB_FLAG_RECOMPUTE_ACT = 0x4
 
 # Every symbol include/mlpb.h declares.
 EXPORTED = (

@@ -175,18 +175,27 @@ def mlp_forward(X, W1, b1, W2, b2, act="gelu", store=None):
     return out
 
 
-def mlp_backward(X, W1, b1, W2, dY, act="gelu", store=None):
+def mlp_backward(X, W1, b1, W2, dY, act="gelu", store=None, recompute=False):
     """Unsharded backward (recomputes the forward activations itself).
 
     Returns dX [T, H], dW1 (shard-major like W1), dW2 [t, H, Fs], db1 [F] (or
     None without bias), db2 [H].  With ``store``, the derivative uses the stored
     Z (or G, U), dW2 the stored A, and dZ is stored before its three uses.
+
+    ``recompute`` (selective activation recomputation, [Concept] §Key math): dW2 uses
+    A recomputed from the stored Z (or G, U) instead of the A the forward kept, i.e.
+    store(act(store(Z))).  Without ``store`` the two are the same number.
     """
     S = store or _identity
     X, b1, dY = _f64(X), _f64(b1), _f64(dY)
     t = np.asarray(W2).shape[0]
     fwd = mlp_forward(X, W1, b1, W2, None, act, store)
     A = fwd["A"]
+    if recompute:
+        if act == "swiglu":
+            A = S(silu(fwd["G"]) * fwd["U"])
+        else:
+            A = S(_POINTWISE[act][0](fwd["Z"]))
     W2f = full_w2(W2)
     db2 = dY.sum(axis=0)
     dA = dY @ W2f

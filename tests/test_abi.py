@@ -65,7 +65,8 @@ def test_accumulate_flag_passes_config_validation(lib):
     that validation accepts shows as not-EINVAL and an unknown one as EINVAL."""
     for flags, ok in ((mlpb.MLPB_FLAG_ACCUMULATE_GRADS, True),
                       (mlpb.MLPB_FLAG_ACCUMULATE_GRADS | mlpb.MLPB_FLAG_FAULT_INJECT, True),
-                      (0x4, False)):
+                      (mlpb.MLPB_FLAG_RECOMPUTE_ACT, True),
+                      (0x8, False)):
         cfg = mlpb.make_config(128, 256, 1024, 2, "gelu", True, flags=flags)
         h = ctypes.c_void_p()
         st = lib.mlpb_create(ctypes.byref(cfg), ctypes.byref(h))
@@ -78,7 +79,8 @@ def test_accumulate_flag_passes_config_validation(lib):
 
 def test_header_flag_values_match_binding():
     src = open(os.path.join(ROOT, "include", "mlpb.h")).read()
-    for name in ("MLPB_FLAG_FAULT_INJECT", "MLPB_FLAG_ACCUMULATE_GRADS"):
+    for name in ("MLPB_FLAG_FAULT_INJECT", "MLPB_FLAG_ACCUMULATE_GRADS",
+                 "MLPB_FLAG_RECOMPUTE_ACT"):
         m = re.search(rf"#define\s+{name}\s+(0x[0-9a-fA-F]+)u", src)
         assert m and int(m.group(1), 16) == getattr(mlpb, name), name
 

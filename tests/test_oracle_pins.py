@@ -23,6 +23,7 @@ import pytest
 
 from oracle import layernorm as ln
 from oracle import mlp
+from oracle.bf16 import round_bf16
 
 RNG = np.random.default_rng(1234)
 
@@ -350,6 +351,38 @@ def test_block_backward_matches_finite_differences():
             lm = loss()
             flat[k] = old
             assert abs((lp - lm) / (2 * h) - gflat[k]) < 1e-6 * max(1.0, abs(gflat[k]))
+
+
+# ------------------------------------------------------------------ selective recomputation
+@pytest.mark.parametrize("act,bias", [("gelu", True), ("swiglu", False)])
+def test_recompute_changes_only_dW2_and_only_by_rounding(act, bias):
+    """Recomputing A from the stored Z moves dW2 by bf16 rounding alone and touches no
+    other gradient; in exact arithmetic it changes nothing."""
+    d = _mlp_inputs(16, 32, 64, 2, act, bias, seed=71)
+    a = (d["X"], d["W1"], d["b1"], d["W2"], d["dY"], act)
+    for store in (None, round_bf16):
+        keep = mlp.mlp_backward(*a, store=store)
+        re = mlp.mlp_backward(*a, store=store, recompute=True)
+        for k in ("dX", "dW1", "db1", "db2"):
+            if keep[k] is not None:
+                assert np.array_equal(keep[k], re[k]), (k, store)
+        diff = re["dW2"] - keep["dW2"]
+        rel = np.sqrt(np.mean(diff ** 2) / np.mean(keep["dW2"] ** 2))
+        if store is None:
+            assert rel == 0.0
+        else:
+            # a few bf16 units of A per term (RMS); a wrong activation is O(1) away
+            assert 0.0 < rel < 1e-2, rel
+
+
+def test_recompute_with_identity_activation_is_exact_under_rounding():
+    """act = identity: A = store(Z) either way (rounding is idempotent), so the
+    recomputed dW2 equals the kept one exactly."""
+    d = _mlp_inputs(8, 16, 32, 2, "identity", True, seed=72)
+    a = (d["X"], d["W1"], d["b1"], d["W2"], d["dY"], "identity")
+    keep = mlp.mlp_backward(*a, store=round_bf16)
+    re = mlp.mlp_backward(*a, store=round_bf16, recompute=True)
+    assert np.array_equal(keep["dW2"], re["dW2"])
 
 
 # ------------------------------------------------------------------ pre-norm MLP branch
