@@ -94,8 +94,8 @@ struct mlpb_handle {
   int db2_splits, db1_splits;
   int64_t db2_rows, db1_rows;
   int ln_blocks_per_shard;
-  // second stream of the backward: the weight gradients and bias sums that do not
-  // depend on each other run beside the dgrad / dX GEMMs and fill their tails
+  // second stream of the backward: db2 at the fork, then (after dgrad) dW2, db1 and dW1
+  // beside dX, filling the GEMMs' tails
   cudaStream_t side;
   cudaEvent_t ev_fork, ev_dz, ev_join;
   // timing
@@ -454,7 +454,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   // CUDA-event interval is its own and not shared with a concurrent one.
   cudaStream_t s2 = h->timing ? s : h->side;
 
-  // Fork: stream s2 starts with everything that needs only dY and A.
+  // Fork: stream s2 starts with db2, which needs only dY; after dgrad it runs dW2, db1, dW1.
   if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
       cudaStreamWaitEvent(s2, h->ev_fork, 0) != cudaSuccess)
     return MLPB_ECUDA;
@@ -469,8 +469,9 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     st = from_cuda(e);
   }
 
-  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T).  With recomputation A is
-  // rewritten by the dgrad epilogue below, so dW2 runs after it.
+  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T), launched after dgrad (below):
+  // with recomputation the dgrad epilogue rewrites A first, and without it the same order
+  // (dW2 and dW1 beside dX, nothing beside dgrad) measured faster on the SwiGLU workloads.
   auto run_dw2 = [&]() -> mlpb_status {
     CUtensorMap ta, tb;
     GemmParams p = base_params(h);
@@ -491,7 +492,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
                     2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   };
   const bool recompute = h->recompute;
-  if (st == MLPB_OK && !recompute) st = run_dw2();
 
   // ---- [s] dgrad of fc2 with the fused activation derivative: dZ [T][F1]
   if (st == MLPB_OK) {
@@ -518,7 +518,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   if (st == MLPB_OK && (cudaEventRecord(h->ev_dz, s) != cudaSuccess ||
                         cudaStreamWaitEvent(s2, h->ev_dz, 0) != cudaSuccess))
     st = MLPB_ECUDA;
-  if (st == MLPB_OK && recompute) st = run_dw2();
+  if (st == MLPB_OK) st = run_dw2();
 
   // ---- [s2] db1 = sum_t dZ
   if (st == MLPB_OK && bias) {
