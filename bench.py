@@ -30,6 +30,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+FP8_OVER_BF16 = 2.0  # nominal dense E4M3 / bf16 tensor throughput on GB300
 METRIC = "MLP-block fwd+bwd TFLOP/s (bf16) on 1 GB300 and fraction of dense bf16 peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = 3
@@ -52,6 +53,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--branch", action="store_true",
                    help="the pre-norm MLP branch with its residual (SP-LN workloads)")
+    p.add_argument("--fp8", action="store_true",
+                   help="E4M3 GEMM operands with per-tensor power-of-two scales")
     p.add_argument("--recompute", action="store_true",
                    help="recompute the activation output in the backward (keep only Z)")
     p.add_argument("--grad-accum", action="store_true",
@@ -79,19 +82,20 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def config_of(shape, wid, grad_accum=False, branch=False, recompute=False):
+def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=False):
     return {"workload": (shape.name or f"workload {wid}") + (" + residual" if branch else ""),
             "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
             "activation": shape.act, "bias": shape.bias, "sp_layernorm": shape.sp_ln,
             "residual_branch": bool(branch), "grad_accum": bool(grad_accum),
             "recompute_act": bool(recompute),
+            "gemm_operands": "e4m3 (per-tensor power-of-two scales)" if fp8 else "bf16",
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_step_fn(shape, wid, tokens, grad_accum=False, branch=False):
+def oracle_step_fn(shape, wid, tokens, grad_accum=False, branch=False, fp8=False):
     """One fwd+bwd of the fp64 oracle on the first `tokens` rows of the workload (adding
     the parameter gradients into carried main-grad buffers with `grad_accum`)."""
     import numpy as np
@@ -104,7 +108,15 @@ def oracle_step_fn(shape, wid, tokens, grad_accum=False, branch=False):
     main = {}
 
     def step():
-        if branch:
+        if fp8:
+            from oracle import fp8 as ofp8
+            if shape.sp_ln:
+                g = ofp8.block_fp8(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
+                                   f["W2"], f["b2"], f["dY"], shape.act)
+            else:
+                ofp8.mlp_forward_fp8(f["X"], f["W1"], f["b1"], f["W2"], f["b2"], shape.act)
+                g = ofp8.mlp_backward_fp8(f["X"], f["W1"], f["b1"], f["W2"], f["dY"], shape.act)
+        elif branch:
             oln.branch_forward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"], f["b1"],
                                f["W2"], f["b2"], shape.act, shape.tp)
             g = oln.branch_backward(f["X"], f["gamma"], f["beta"], shape.ln_eps, f["W1"],
@@ -132,17 +144,17 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(shape, wid, target_s, grad_accum=False, branch=False):
+def cpu_baseline(shape, wid, target_s, grad_accum=False, branch=False, fp8=False):
     """The oracle as it stands, timed on this host's cores on a bounded token sample."""
     tokens = 128
-    step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch)
+    step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch, fp8)
     t0 = time.perf_counter()
     step()
     dt = time.perf_counter() - t0
     reps = max(1, int(target_s / max(dt, 1e-3)))
     if reps > 4 and shape.tokens >= 1024:  # prefer one larger sample to many small ones
         tokens = min(shape.tokens, 128 * min(8, reps // 2))
-        step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch)
+        step, flops = oracle_step_fn(shape, wid, tokens, grad_accum, branch, fp8)
         t0 = time.perf_counter()
         step()
         dt = time.perf_counter() - t0
@@ -168,7 +180,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     shape = bench_shape(args)
-    step, flops = oracle_step_fn(shape, args.workload, 128, args.grad_accum, args.branch)
+    step, flops = oracle_step_fn(shape, args.workload, 128, args.grad_accum, args.branch,
+                                 args.fp8)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -181,7 +194,7 @@ def run_reference(args, rank, world):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
            "config": config_of(shape, args.workload, args.grad_accum, args.branch,
-                               args.recompute),
+                               args.recompute, args.fp8),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                             "sample": f"each step: fwd+bwd of the fp64 oracle on the first 128 "
                                       f"of {shape.tokens} tokens"},
@@ -284,13 +297,15 @@ def run_native(args, rank, world, local_rank):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, args.workload, args.cpu_seconds, args.grad_accum,
-                           args.branch)
+                           args.branch, args.fp8)
 
     d = make_inputs(shape, args.workload)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     flags = mlpb.MLPB_FLAG_ACCUMULATE_GRADS if args.grad_accum else 0
     if args.recompute:
         flags |= mlpb.MLPB_FLAG_RECOMPUTE_ACT
+    if args.fp8:
+        flags |= mlpb.MLPB_FLAG_FP8
     if args.branch:
         blk = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
                              shape.bias, shape.ln_eps, flags)
@@ -406,7 +421,13 @@ def run_native(args, rank, world, local_rank):
         kernels.append(row)
     top = kernels[0]
     topk = per[top["name"]]
-    if topk["flops"] > 0:
+    if topk["flops"] > 0 and top["name"].endswith("_f8"):
+        achieved = topk["flops"] / (top["avg_ms"] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": top["name"], "achieved": achieved,
+                    "peak": FP8_OVER_BF16 * peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "peak_source": f"{peak_src} sustained dense bf16 x {FP8_OVER_BF16} (nominal "
+                                   "dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)"}
+    elif topk["flops"] > 0:
         achieved = topk["flops"] / (top["avg_ms"] * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": top["name"], "achieved": achieved,
                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
@@ -425,9 +446,10 @@ def run_native(args, rank, world, local_rank):
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-               "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+               "dtype": "e4m3" if args.fp8 else "bf16",
+               "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
                "config": config_of(shape, args.workload, args.grad_accum, args.branch,
-                               args.recompute),
+                               args.recompute, args.fp8),
                "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
                "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
                "roofline": roofline, "kernels": kernels,

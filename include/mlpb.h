@@ -98,6 +98,18 @@ typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
  * forward writes it for fc2, the backward rewrites it).  A is recomputed from the
  * bf16-rounded Z, so dW2 can differ from the stored-A path by bf16 rounding. */
 #define MLPB_FLAG_RECOMPUTE_ACT 0x4u
+/* FP8 GEMMs ("Why Megatron-LM Matters" / "Key Features" of the onegen.ai page: mixed
+ * precision down to FP8; the concept note's "Key math": FP8 through Transformer Engine).
+ * All six GEMMs of mlpb_forward / mlpb_backward run on E4M3 operands (tcgen05
+ * kind::f8f6f4, fp32 accumulation) with per-tensor current scaling: each operand tensor
+ * (X, W1, W2, A, dY, dZ; every shard at once) gets the power-of-two scale of
+ * mlpb_quantize_e4m3 from its own absolute maximum, and each GEMM rescales its sums by
+ * the inverse of its two operands' scales.  Everything else keeps the bf16 path's
+ * precision: Z (G, U), A and dZ are bf16, Y, dX and the parameter gradients fp32, the
+ * bias sums and the LayerNorm unchanged.  The workspace (mlpb_workspace_size) then also
+ * holds the E4M3 copies and is required by mlpb_forward too.  Requires F/tp % 16 == 0;
+ * not combined with MLPB_FLAG_RECOMPUTE_ACT. */
+#define MLPB_FLAG_FP8 0x8u
 
 typedef struct {
   int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */
@@ -242,6 +254,20 @@ mlpb_status mlpb_read_timings(mlpb_handle *h, mlpb_kernel_time *out, int capacit
  * rows may be 0 (out becomes zeros, `in` may then be NULL).  Allocates nothing. */
 mlpb_status mlpb_bias_grad_noalloc(const void *in, int64_t rows, int64_t cols, float *out,
                                    mlpb_stream_t stream);
+
+/* E4M3 quantization of a bf16 tensor [batches][rows][cols] with one power-of-two scale
+ * for the whole tensor (the FP8 recipe of MLPB_FLAG_FP8; "Why Megatron-LM Matters" and
+ * "Key Features" of the onegen.ai page name FP8 mixed precision, the concept note's "Key
+ * math" FP8 through Transformer Engine).  With amax the largest |x| and k the largest
+ * integer such that amax * 2^k <= 448, each code is e4m3(x * 2^k), round to nearest even
+ * (x * 2^k is exact).  Writes q [batches][rows][cols] and/or qt [batches][cols][rows]
+ * (the transposed codes; either may be NULL, not both), *amax = the fp32 bit pattern of
+ * the tensor's largest magnitude (device word, overwritten), and *scale_exp = k (device
+ * int, may be NULL).  rows % 16 == 0, cols % 16 == 0, 16-byte aligned tensors, 4-byte
+ * aligned words.  Allocates nothing; no handle. */
+mlpb_status mlpb_quantize_e4m3(const void *in, int64_t batches, int64_t rows, int64_t cols,
+                               void *q, void *qt, uint32_t *amax, int32_t *scale_exp,
+                               mlpb_stream_t stream);
 
 /* Static English text of a status code. */
 const char *mlpb_status_str(mlpb_status s);

@@ -11,6 +11,7 @@ from .mlp_inputs import (  # noqa: F401
     make_inputs,
     make_ln_grad,
     make_main_grads,
+    make_bf16,
     sample_rows,
     sample_ffn_cols,
     reduced_tokens,

@@ -131,6 +131,18 @@ def make_main_grads(shapes: dict, wid: int, scales: dict | None = None) -> dict:
     return out
 
 
+def make_bf16(shape, seed: int, std: float = 1.0, log2_spread: int = 0) -> torch.Tensor:
+    """A seeded bf16 tensor: N(0, std^2) values, each multiplied by 2^u with u uniform
+    on the integers [-log2_spread, log2_spread] (a wide dynamic range when > 0)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(SEED_BASE + 7919 * seed)
+    x = torch.randn(shape, generator=g, dtype=torch.float32) * std
+    if log2_spread:
+        e = torch.randint(-log2_spread, log2_spread + 1, shape, generator=g)
+        x = torch.ldexp(x, e)
+    return x.to(torch.bfloat16)
+
+
 def reduced_tokens(shape: MLPShape, tokens: int = 512) -> MLPShape:
     """Same H, F, t and activation with fewer tokens (a multiple of 128 and of t)."""
     return shape.with_tokens(min(shape.tokens, tokens))

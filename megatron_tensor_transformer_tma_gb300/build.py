@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmlpb.so")
 SOURCES = ["api.cu", "gemm_fwd.cu", "gemm_bwd.cu", "reduce.cu", "layernorm.cu",
-           "reduce_noalloc.cu"]
+           "reduce_noalloc.cu", "fp8.cu", "gemm_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]

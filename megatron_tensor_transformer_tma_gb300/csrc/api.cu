@@ -61,6 +61,41 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+// An E4M3 operand map (one-byte elements, 128-byte swizzle, boxes 128 elements deep).
+bool encode_u8(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+               const uint64_t* strides_bytes, const uint32_t* box) {
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int k = 0; k < rank; ++k) {
+    gd[k] = dims[k];
+    bx[k] = box[k];
+    es[k] = 1;
+    if (k + 1 < rank) gs[k] = strides_bytes[k];
+  }
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// [outer][inner] E4M3, K-major tiles of 128 x 128.
+bool map_u8(CUtensorMap* m, const void* p, uint64_t inner, uint64_t outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t str[1] = {inner};
+  const uint32_t box[2] = {128, 128};
+  return encode_u8(m, p, 2, dims, str, box);
+}
+
+// [t][rows][inner] E4M3 as a 3-D map {inner, rows, t}, tiles of 128 x 128 in one shard.
+bool map_u8_sharded(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows, uint64_t t,
+                    uint64_t row_stride, uint64_t shard_stride) {
+  const uint64_t dims[3] = {inner, rows, t};
+  const uint64_t str[2] = {row_stride, shard_stride};
+  const uint32_t box[3] = {128, 128, 1};
+  return encode_u8(m, p, 3, dims, str, box);
+}
+
 bool map2d(CUtensorMap* m, const void* p, uint64_t inner, uint64_t outer, uint64_t ld_elems,
            uint32_t box_inner, uint32_t box_outer) {
   const uint64_t dims[2] = {inner, outer};
@@ -89,6 +124,7 @@ struct mlpb_handle {
   bool fault_pending;
   bool accumulate;  // MLPB_FLAG_ACCUMULATE_GRADS: parameter gradients add into their outputs
   bool recompute;   // MLPB_FLAG_RECOMPUTE_ACT: the backward rewrites A from the saved Z
+  bool fp8;         // MLPB_FLAG_FP8: E4M3 GEMMs, per-tensor power-of-two scales
   uint64_t wait_ns;
   // bias-grad split plans
   int db2_splits, db1_splits;
@@ -169,6 +205,37 @@ mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap&
   return from_cuda(e);
 }
 
+mlpb_status run_gemm_f8(mlpb_handle* h, GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                        const GemmParams& p, cudaStream_t s, const char* name, double flops,
+                        double bytes) {
+  const int super_tiles = static_cast<int>(cdiv(p.num_m_tiles, kClusterM)) * p.num_n_tiles;
+  if (super_tiles == 0) return MLPB_OK;
+  const int clusters = std::min(super_tiles, h->max_clusters);
+  LaunchTimer lt(h, s, name, flops, bytes);
+  cudaError_t e = launch_gemm_f8(kind, a, b, p, clusters, s);
+  lt.done();
+  return from_cuda(e);
+}
+
+// amax of a bf16 tensor of n elements into *slot (which must start at zero).
+mlpb_status f8_amax(mlpb_handle* h, const void* x, int64_t n, uint32_t* slot, cudaStream_t s,
+                    const char* name) {
+  LaunchTimer lt(h, s, name, 0.0, 2.0 * n);
+  cudaError_t e = launch_amax_bf16(x, n, slot, h->num_sms, s);
+  lt.done();
+  return from_cuda(e);
+}
+
+// E4M3 copies of a bf16 [batches][R][C] tensor: q (same layout) and/or qt (transposed).
+mlpb_status f8_cast(mlpb_handle* h, const void* x, int batches, int64_t R, int64_t C, void* q,
+                    void* qt, const uint32_t* slot, cudaStream_t s, const char* name) {
+  const double n = static_cast<double>(batches) * R * C;
+  LaunchTimer lt(h, s, name, 0.0, n * (2.0 + (q ? 1.0 : 0.0) + (qt ? 1.0 : 0.0)));
+  cudaError_t e = launch_cast_e4m3(x, batches, R, C, q, qt, slot, nullptr, s);
+  lt.done();
+  return from_cuda(e);
+}
+
 size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
 
 size_t ws_backward_bytes(const mlpb_handle* h) {
@@ -184,6 +251,55 @@ size_t ws_ln_bytes(const mlpb_handle* h) {
   if (!h->cfg.seq_parallel_ln) return 0;
   const size_t nblk = static_cast<size_t>(h->t) * h->ln_blocks_per_shard;
   return 2 * align256(nblk * h->H * 4);
+}
+
+// FP8 region of the workspace, after the bf16 path's scratch: the amax words, then the
+// E4M3 copies of the six GEMM operands, each in its own layout and transposed.
+enum F8Amax { kAmaxX = 0, kAmaxW1, kAmaxW2, kAmaxA, kAmaxDY, kAmaxDZ, kAmaxWords = 8 };
+struct F8Layout {
+  uint32_t* amax;
+  uint8_t *Xq, *Xt, *W1q, *W1t, *W2q, *W2t, *Aq, *At, *dYq, *dYt, *dZq, *dZt;
+};
+
+size_t ws_base_bytes(const mlpb_handle* h) {
+  return align256(std::max<size_t>(std::max(ws_backward_bytes(h), ws_ln_bytes(h)), 256));
+}
+
+size_t ws_f8_bytes(const mlpb_handle* h) {
+  if (!h->fp8) return 0;
+  const size_t TH = static_cast<size_t>(h->T * h->H), F1H = static_cast<size_t>(h->F1 * h->H),
+               FH = static_cast<size_t>(h->F * h->H), TF = static_cast<size_t>(h->T * h->F),
+               TF1 = static_cast<size_t>(h->T * h->F1);
+  return 256 + 2 * (align256(TH) + align256(F1H) + align256(FH) + align256(TF) + align256(TH) +
+                    align256(TF1));
+}
+
+F8Layout f8_layout(const mlpb_handle* h, void* workspace) {
+  uint8_t* b = static_cast<uint8_t*>(workspace) + ws_base_bytes(h);
+  F8Layout L;
+  L.amax = reinterpret_cast<uint32_t*>(b);
+  b += 256;
+  auto take = [&b](size_t n) {
+    uint8_t* p = b;
+    b += align256(n);
+    return p;
+  };
+  const size_t TH = static_cast<size_t>(h->T * h->H), F1H = static_cast<size_t>(h->F1 * h->H),
+               FH = static_cast<size_t>(h->F * h->H), TF = static_cast<size_t>(h->T * h->F),
+               TF1 = static_cast<size_t>(h->T * h->F1);
+  L.Xq = take(TH);
+  L.Xt = take(TH);
+  L.W1q = take(F1H);
+  L.W1t = take(F1H);
+  L.W2q = take(FH);
+  L.W2t = take(FH);
+  L.Aq = take(TF);
+  L.At = take(TF);
+  L.dYq = take(TH);
+  L.dYt = take(TH);
+  L.dZq = take(TF1);
+  L.dZt = take(TF1);
+  return L;
 }
 
 void plan_colsum(int64_t R, int64_t C, int num_sms, int* splits, int64_t* rows) {
@@ -220,12 +336,15 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   if (c.has_bias != 0 && c.has_bias != 1) return MLPB_EINVAL;
   if (c.seq_parallel_ln != 0 && c.seq_parallel_ln != 1) return MLPB_EINVAL;
   if ((c.flags & ~(MLPB_FLAG_FAULT_INJECT | MLPB_FLAG_ACCUMULATE_GRADS |
-                   MLPB_FLAG_RECOMPUTE_ACT)) != 0)
+                   MLPB_FLAG_RECOMPUTE_ACT | MLPB_FLAG_FP8)) != 0)
     return MLPB_EINVAL;
   if (c.seq_parallel_ln && !(c.ln_eps > 0.f)) return MLPB_EINVAL;
   if (c.tokens % 128 != 0 || c.hidden % 64 != 0) return MLPB_EUNSUPPORTED;
   if (c.ffn % c.tp != 0 || (c.ffn / c.tp) % 8 != 0) return MLPB_EUNSUPPORTED;
   if (c.act == MLPB_ACT_SWIGLU && c.has_bias) return MLPB_EUNSUPPORTED;
+  if ((c.flags & MLPB_FLAG_FP8) &&
+      ((c.ffn / c.tp) % 16 != 0 || (c.flags & MLPB_FLAG_RECOMPUTE_ACT)))
+    return MLPB_EUNSUPPORTED;  // E4M3 rows must be 16-byte multiples for TMA
   if (c.seq_parallel_ln && (c.tokens % c.tp != 0 || c.hidden > 16384)) return MLPB_EUNSUPPORTED;
   const int64_t f1 = c.act == MLPB_ACT_SWIGLU ? 2 * c.ffn : c.ffn;
   // int32 tile/coordinate arithmetic inside the kernels
@@ -245,6 +364,7 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   h->fault_pending = (c.flags & MLPB_FLAG_FAULT_INJECT) != 0;
   h->accumulate = (c.flags & MLPB_FLAG_ACCUMULATE_GRADS) != 0;
   h->recompute = (c.flags & MLPB_FLAG_RECOMPUTE_ACT) != 0;
+  h->fp8 = (c.flags & MLPB_FLAG_FP8) != 0;
   h->wait_ns = 1000000000ull;
   h->timing = false;
   h->d_err = nullptr;
@@ -264,6 +384,7 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   }
   if (load_encoder() != MLPB_OK || gemm_fwd_set_smem_attrs() != cudaSuccess ||
       gemm_bwd_set_smem_attrs() != cudaSuccess ||
+      (h->fp8 && gemm_f8_set_smem_attrs() != cudaSuccess) ||
       cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
     if (h->d_err) cudaFree(h->d_err);
@@ -311,7 +432,8 @@ void mlpb_destroy(mlpb_handle* h) {
 
 mlpb_status mlpb_workspace_size(const mlpb_handle* h, size_t* bytes) {
   if (h == nullptr || bytes == nullptr) return MLPB_EINVAL;
-  *bytes = std::max<size_t>(std::max(ws_backward_bytes(h), ws_ln_bytes(h)), 256);
+  *bytes = h->fp8 ? ws_base_bytes(h) + ws_f8_bytes(h)
+                  : std::max<size_t>(std::max(ws_backward_bytes(h), ws_ln_bytes(h)), 256);
   return MLPB_OK;
 }
 
@@ -324,7 +446,12 @@ mlpb_status mlpb_saved_size(const mlpb_handle* h, size_t* z_bytes, size_t* a_byt
 
 static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
                                 const void* W2, const void* b2, float* Y, void* Zsaved,
-                                void* Asaved, const void* resid, cudaStream_t s);
+                                void* Asaved, const void* resid, void* workspace,
+                                cudaStream_t s);
+static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, const void* W2,
+                               const void* Zsaved, const void* Asaved, const void* dY,
+                               float* dX, float* dW1, float* dW2, float* db1, float* db2,
+                               void* workspace, cudaStream_t s);
 static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
                                const float* mean, const float* rstd, const float* dXn,
                                const void* dres, float* dX, float* dgamma, float* dbeta,
@@ -333,25 +460,103 @@ static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
 mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const void* b1,
                          const void* W2, const void* b2, float* Y, void* Zsaved, void* Asaved,
                          void* workspace, mlpb_stream_t stream) {
-  (void)workspace;
   if (h == nullptr) return MLPB_EINVAL;
   const bool bias = h->cfg.has_bias != 0;
   if (!W1 || !W2) return MLPB_EINVAL;
   if (h->T > 0 && (!X || !Y || !Zsaved || !Asaved)) return MLPB_EINVAL;  // T = 0: empty tensors
+  if (h->T > 0 && h->fp8 && (!workspace || !aligned16(workspace))) return MLPB_EINVAL;
   if (bias != (b1 != nullptr) || bias != (b2 != nullptr)) return MLPB_EINVAL;
   for (const void* p : {X, W1, W2, static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
                         static_cast<const void*>(Asaved), b1, b2})
     if (p && !aligned16(p)) return MLPB_EINVAL;
   if (h->T == 0) return MLPB_OK;
-  return forward_impl(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, nullptr,
+  return forward_impl(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, nullptr, workspace,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 // fc1 and fc2 of a validated forward; `resid` (bf16 [T][H] or NULL) is added to Y in
 // fc2's epilogue after b2.
+// The forward with E4M3 GEMMs: amax and E4M3 copies of X, W1, W2; fc1 (records amax(A));
+// the E4M3 copy of A; fc2.
+static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                              const void* W2, const void* b2, float* Y, void* Zsaved,
+                              void* Asaved, const void* resid, void* workspace, cudaStream_t s) {
+  const bool bias = h->cfg.has_bias != 0;
+  const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
+  const F8Layout L = f8_layout(h, workspace);
+  uint32_t* am = L.amax;
+  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess) return MLPB_ECUDA;
+  mlpb_status st = f8_amax(h, X, T * H, am + kAmaxX, s, "fp8_amax_x");
+  if (st == MLPB_OK) st = f8_amax(h, W1, F1 * H, am + kAmaxW1, s, "fp8_amax_w1");
+  if (st == MLPB_OK) st = f8_amax(h, W2, F * H, am + kAmaxW2, s, "fp8_amax_w2");
+  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, L.Xq, nullptr, am + kAmaxX, s, "fp8_cast_x");
+  if (st == MLPB_OK)
+    st = f8_cast(h, W1, 1, F1, H, L.W1q, nullptr, am + kAmaxW1, s, "fp8_cast_w1");
+  if (st == MLPB_OK)
+    st = f8_cast(h, W2, 1, t * H, Fs, L.W2q, nullptr, am + kAmaxW2, s, "fp8_cast_w2");
+  if (st != MLPB_OK) return st;
+
+  // ---- fc1
+  CUtensorMap ta, tb;
+  GemmParams p = base_params(h);
+  p.M = static_cast<int>(T);
+  p.num_m_tiles = static_cast<int>(T / kBM);
+  p.num_kb = static_cast<int>(cdiv(H, kBK8));
+  p.out0 = Zsaved;
+  p.out1 = Asaved;
+  p.amax_a = am + kAmaxX;
+  p.amax_b = am + kAmaxW1;
+  p.amax_out = am + kAmaxA;
+  p.fault_inject = h->fault_pending ? 1 : 0;
+  h->fault_pending = false;
+  if (!map_u8(&ta, L.Xq, H, T)) return MLPB_EINVAL;
+  if (!h->swiglu) {
+    if (!map_u8(&tb, L.W1q, H, F)) return MLPB_EINVAL;
+    p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
+    p.bias = static_cast<const __nv_bfloat16*>(b1);
+    st = run_gemm_f8(h, GemmKind::FC1_GELU, ta, tb, p, s, "fc1_gelu_f8", 2.0 * T * F * H,
+                     1.0 * (T * H + F * H) + 4.0 * T * F + (bias ? 2.0 * F : 0.0));
+  } else {
+    const uint64_t dims[4] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs), 2,
+                              static_cast<uint64_t>(t)};
+    const uint64_t str[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs * H),
+                             static_cast<uint64_t>(2 * Fs * H)};
+    const uint32_t box[4] = {128, 128, 1, 1};
+    if (!encode_u8(&tb, L.W1q, 4, dims, str, box)) return MLPB_EINVAL;
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    st = run_gemm_f8(h, GemmKind::FC1_SWIGLU, ta, tb, p, s, "fc1_swiglu_f8", 4.0 * T * F * H,
+                     1.0 * (T * H + 2 * F * H) + 6.0 * T * F);
+  }
+  if (st == MLPB_OK)
+    st = f8_cast(h, Asaved, 1, T, F, L.Aq, nullptr, am + kAmaxA, s, "fp8_cast_a");
+  if (st != MLPB_OK) return st;
+
+  // ---- fc2 (the sum over shards accumulates in one TMEM tile; one scale for all shards)
+  if (!map_u8_sharded(&ta, L.Aq, Fs, T, t, F, Fs) ||
+      !map_u8_sharded(&tb, L.W2q, Fs, H, t, Fs, H * Fs))
+    return MLPB_EINVAL;
+  GemmParams q = base_params(h);
+  q.M = static_cast<int>(T);
+  q.num_m_tiles = static_cast<int>(T / kBM);
+  q.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+  q.kb_per_shard = static_cast<int>(cdiv(Fs, kBK8));
+  q.num_kb = static_cast<int>(t * q.kb_per_shard);
+  q.bias = static_cast<const __nv_bfloat16*>(b2);
+  q.aux = static_cast<const __nv_bfloat16*>(resid);
+  q.out0 = Y;
+  q.amax_a = am + kAmaxA;
+  q.amax_b = am + kAmaxW2;
+  return run_gemm_f8(h, GemmKind::FC2, ta, tb, q, s, "fc2_f8", 2.0 * T * H * F,
+                     1.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
+                         (resid ? 2.0 * T * H : 0.0));
+}
+
 static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
                                 const void* W2, const void* b2, float* Y, void* Zsaved,
-                                void* Asaved, const void* resid, cudaStream_t s) {
+                                void* Asaved, const void* resid, void* workspace,
+                                cudaStream_t s) {
+  if (h->fp8) return forward_f8(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, resid, workspace, s);
   const bool bias = h->cfg.has_bias != 0;
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t;
 
@@ -445,6 +650,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     return st;
   }
 
+  if (h->fp8)
+    return backward_f8(h, X, W1, W2, Zsaved, Asaved, dY, dX, dW1, dW2, db1, db2, workspace, s);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* dZ = ws;
   float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
@@ -567,6 +774,127 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   return st;
 }
 
+// The backward with E4M3 GEMMs, on the caller's stream: amax of dY, W2, X, W1, A; E4M3
+// copies (dY both ways, W2 transposed); dgrad (records amax(dZ)); the bias sums; E4M3
+// copies of dZ (both ways), W1, X and A (transposed); dX, dW2, dW1.
+static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, const void* W2,
+                               const void* Zsaved, const void* Asaved, const void* dY,
+                               float* dX, float* dW1, float* dW2, float* db1, float* db2,
+                               void* workspace, cudaStream_t s) {
+  const bool bias = h->cfg.has_bias != 0;
+  const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
+  const int acc = h->accumulate ? 1 : 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* dZ = ws;
+  float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
+  float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
+                                          align256(static_cast<size_t>(h->db2_splits) * H * 4));
+  const F8Layout L = f8_layout(h, workspace);
+  uint32_t* am = L.amax;
+  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess) return MLPB_ECUDA;
+  mlpb_status st = f8_amax(h, dY, T * H, am + kAmaxDY, s, "fp8_amax_dy");
+  if (st == MLPB_OK) st = f8_amax(h, W2, F * H, am + kAmaxW2, s, "fp8_amax_w2");
+  if (st == MLPB_OK) st = f8_amax(h, X, T * H, am + kAmaxX, s, "fp8_amax_x");
+  if (st == MLPB_OK) st = f8_amax(h, W1, F1 * H, am + kAmaxW1, s, "fp8_amax_w1");
+  if (st == MLPB_OK) st = f8_amax(h, Asaved, T * F, am + kAmaxA, s, "fp8_amax_a");
+  if (st == MLPB_OK)
+    st = f8_cast(h, dY, 1, T, H, L.dYq, L.dYt, am + kAmaxDY, s, "fp8_cast_dy");
+  if (st == MLPB_OK)
+    st = f8_cast(h, W2, static_cast<int>(t), H, Fs, nullptr, L.W2t, am + kAmaxW2, s,
+                 "fp8_cast_w2t");
+  if (st != MLPB_OK) return st;
+  CUtensorMap ta, tb;
+
+  // ---- dgrad of fc2 with the fused activation derivative: dZ [T][F1] bf16
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(T);
+    p.num_m_tiles = static_cast<int>(T / kBM);
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_kb = static_cast<int>(cdiv(H, kBK8));
+    p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
+    p.out0 = dZ;
+    p.amax_a = am + kAmaxDY;
+    p.amax_b = am + kAmaxW2;
+    p.amax_out = am + kAmaxDZ;
+    if (!map_u8(&ta, L.dYq, H, T) || !map_u8_sharded(&tb, L.W2t, H, Fs, t, H, Fs * H))
+      return MLPB_EINVAL;
+    st = run_gemm_f8(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, ta, tb, p, s,
+                     h->swiglu ? "dgrad_swiglu_f8" : "dgrad_gelu_f8", 2.0 * T * F * H,
+                     1.0 * (T * H + F * H) + 4.0 * T * F1);
+  }
+  // ---- bias sums on the bf16 dY and dZ
+  if (st == MLPB_OK && bias) {
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H, 2);
+    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s, acc);
+    lt.done();
+    st = from_cuda(e);
+    if (st == MLPB_OK) {
+      LaunchTimer lt1(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
+      e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s, acc);
+      lt1.done();
+      st = from_cuda(e);
+    }
+  }
+  if (st == MLPB_OK)
+    st = f8_cast(h, dZ, 1, T, F1, L.dZq, L.dZt, am + kAmaxDZ, s, "fp8_cast_dz");
+  if (st == MLPB_OK)
+    st = f8_cast(h, W1, 1, F1, H, nullptr, L.W1t, am + kAmaxW1, s, "fp8_cast_w1t");
+  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, nullptr, L.Xt, am + kAmaxX, s, "fp8_cast_xt");
+  if (st == MLPB_OK)
+    st = f8_cast(h, Asaved, 1, T, F, nullptr, L.At, am + kAmaxA, s, "fp8_cast_at");
+  if (st != MLPB_OK) return st;
+
+  // ---- dX = sum_i dZ_i W1_i (f backward: the K loop runs over every shard's rows)
+  {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(T);
+    p.num_m_tiles = static_cast<int>(T / kBM);
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    p.num_kb = static_cast<int>(cdiv(F1, kBK8));
+    p.out0 = dX;
+    p.amax_a = am + kAmaxDZ;
+    p.amax_b = am + kAmaxW1;
+    if (!map_u8(&ta, L.dZq, F1, T) || !map_u8(&tb, L.W1t, F1, H)) return MLPB_EINVAL;
+    st = run_gemm_f8(h, GemmKind::DX, ta, tb, p, s, "dgrad_x_f8", 2.0 * T * H * F1,
+                     1.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+  }
+  // ---- dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
+  if (st == MLPB_OK) {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(H);
+    p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_kb = static_cast<int>(T / kBK8);
+    p.out0 = dW2;
+    p.accumulate = acc;
+    p.amax_a = am + kAmaxDY;
+    p.amax_b = am + kAmaxA;
+    if (!map_u8(&ta, L.dYt, T, H) || !map_u8_sharded(&tb, L.At, T, Fs, t, T, Fs * T))
+      return MLPB_EINVAL;
+    st = run_gemm_f8(h, GemmKind::WGRAD_W2, ta, tb, p, s, "wgrad_w2_f8", 2.0 * H * F * T,
+                     1.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
+  }
+  // ---- dW1 = dZ^T X  (M = F1, N = H, K = T)
+  if (st == MLPB_OK) {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(F1);
+    p.num_m_tiles = static_cast<int>(cdiv(F1, kBM));
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    p.num_kb = static_cast<int>(T / kBK8);
+    p.out0 = dW1;
+    p.accumulate = acc;
+    p.amax_a = am + kAmaxDZ;
+    p.amax_b = am + kAmaxX;
+    if (!map_u8(&ta, L.dZt, T, F1) || !map_u8(&tb, L.Xt, T, H)) return MLPB_EINVAL;
+    st = run_gemm_f8(h, GemmKind::WGRAD_W1, ta, tb, p, s, "wgrad_w1_f8", 2.0 * F1 * H * T,
+                     1.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
+  }
+  return st;
+}
+
 mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle* h, const void* X, const void* gamma,
                                   const void* beta, void* Xn, float* mean, float* rstd,
                                   mlpb_stream_t stream) {
@@ -645,11 +973,11 @@ mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma
                         static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
                         static_cast<const void*>(Asaved), b1, b2})
     if (p && !aligned16(p)) return MLPB_EINVAL;
-  (void)workspace;
+  if (h->T > 0 && h->fp8 && (!workspace || !aligned16(workspace))) return MLPB_EINVAL;
   if (h->T == 0) return MLPB_OK;
   mlpb_status st = mlpb_layernorm_sp_fwd(h, X, gamma, beta, Xn, mean, rstd, stream);
   if (st != MLPB_OK) return st;
-  return forward_impl(h, Xn, W1, b1, W2, b2, Y, Zsaved, Asaved, X,
+  return forward_impl(h, Xn, W1, b1, W2, b2, Y, Zsaved, Asaved, X, workspace,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 

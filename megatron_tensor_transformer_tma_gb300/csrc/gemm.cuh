@@ -17,6 +17,11 @@
 // Every wait is bounded (common.cuh): a wait that expires raises the CTA's abort flag
 // and the device error word; all roles then drain what they issued and free TMEM.
 //
+// The F8 instantiation runs the same pipeline on E4M3 operands (tcgen05 kind::f8f6f4, K = 32
+// a call, 128-byte = 128-element K-major rows, every operand K-major from its own or its
+// transposed E4M3 copy) and rescales each accumulator by 2^-(k_a + k_b) in the epilogue;
+// FC1 and DGRAD also record the amax of the bf16 A / dZ they write.
+//
 // The contractions (T tokens, H hidden, F ffn, t shards, Fs = F/t, F1 = F or 2F):
 //   FC1_GELU      Z = X W1^T + b1, A = gelu(Z)       M=T  N=F      K=H   A,B K-major
 //   FC1_SWIGLU    [G|U] = X [Wg_i|Wu_i]^T, A = silu(G)U  (per shard i, 128 gate + 128 up
@@ -31,6 +36,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "gemm_params.h"
 
 namespace mlpb {
@@ -138,12 +144,29 @@ __device__ __forceinline__ void tmem_load_f32x32(uint32_t taddr, float (&v)[32])
   for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
 }
 
+// One 32-column accumulator chunk; FP8 sums are rescaled by 2^-(k_a + k_b) (sc, exact).
+template <bool F8>
+__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32], float sc) {
+  tmem_load_f32x32(taddr, v);
+  if constexpr (F8) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] *= sc;
+  }
+}
+
+// am = max(am, |v[e]|) over the chunk's valid columns (FP8: amax of a written operand).
+__device__ __forceinline__ void track_amax(const float (&v)[32], int nv, float& am) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (e < nv) am = fmaxf(am, fabsf(v[e]));
+}
+
 // Epilogue of one 128 x 256 tile for the calling thread's row.  `tacc` is the TMEM
 // address of the accumulator at this warp's lane quarter.  All branches that skip
 // tcgen05.ld are uniform across the warp.
-template <GemmKind K>
+template <GemmKind K, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, int nt,
-                                              const GemmParams& p) {
+                                              const GemmParams& p, float sc, float& am) {
   const int m = mt * kBM + row;
   const bool row_ok = m < p.M;
   if constexpr (K == GemmKind::FC1_GELU) {
@@ -155,7 +178,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int col = n0 + c * 32;
       if (col >= p.F) break;
       float v[32];
-      tmem_load_f32x32(tacc + c * 32, v);
+      load_acc<F8>(tacc + c * 32, v, sc);
       const int nv = min(32, p.F - col);
       if (p.bias != nullptr) {
         float b[32];
@@ -166,7 +189,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       if (row_ok) store_bf16x32(Z + col, nv, v);
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
-      if (row_ok) store_bf16x32(A + col, nv, v);
+      if (row_ok) {
+        store_bf16x32(A + col, nv, v);
+        if constexpr (F8) track_amax(v, nv, am);
+      }
     }
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
@@ -180,8 +206,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float g[32], u[32];
-      tmem_load_f32x32(tacc + c * 32, g);
-      tmem_load_f32x32(tacc + 128 + c * 32, u);
+      load_acc<F8>(tacc + c * 32, g, sc);
+      load_acc<F8>(tacc + 128 + c * 32, u, sc);
       const int nv = min(32, p.Fs - jc);
       if (row_ok) {
         store_bf16x32(GU + jc, nv, g);
@@ -189,7 +215,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       }
 #pragma unroll
       for (int e = 0; e < 32; ++e) u[e] *= g[e] * sigmoid_f(g[e]);
-      if (row_ok) store_bf16x32(A + jc, nv, u);
+      if (row_ok) {
+        store_bf16x32(A + jc, nv, u);
+        if constexpr (F8) track_amax(u, nv, am);
+      }
     }
   } else if constexpr (K == GemmKind::FC2 || K == GemmKind::DX) {
     const int n0 = nt * kBN;
@@ -199,7 +228,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
-      tmem_load_f32x32(tacc + c * 32, v);
+      load_acc<F8>(tacc + c * 32, v, sc);
       const int nv = min(32, p.H - col);
       if (K == GemmKind::FC2 && p.bias != nullptr) {
         float b[32];
@@ -228,7 +257,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32], z[32];
-      tmem_load_f32x32(tacc + c * 32, v);
+      load_acc<F8>(tacc + c * 32, v, sc);
       const int nv = min(32, p.Fs - jc);
       if (row_ok) {
         load_bf16x32(Z + jc, nv, z);
@@ -241,6 +270,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
         store_bf16x32(dZ + jc, nv, v);
+        if constexpr (F8) track_amax(v, nv, am);
       }
     }
   } else if constexpr (K == GemmKind::DGRAD_SWIGLU) {
@@ -258,7 +288,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float da[32];
-      tmem_load_f32x32(tacc + c * 32, da);
+      load_acc<F8>(tacc + c * 32, da, sc);
       const int nv = min(32, p.Fs - jc);
       if (row_ok) {
         float g[32], u[32];
@@ -279,6 +309,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         }
         store_bf16x32(dGU + jc, nv, g);
         store_bf16x32(dGU + p.Fs + jc, nv, u);
+        if constexpr (F8) {
+          track_amax(g, nv, am);
+          track_amax(u, nv, am);
+        }
       }
     }
   } else if constexpr (K == GemmKind::WGRAD_W2) {
@@ -290,7 +324,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32];
-      tmem_load_f32x32(tacc + c * 32, v);
+      load_acc<F8>(tacc + c * 32, v, sc);
       if (row_ok) {
         const int nv = min(32, p.Fs - jc);
         if (p.accumulate) add_f32x32(dW + jc, nv, v);
@@ -305,7 +339,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
-      tmem_load_f32x32(tacc + c * 32, v);
+      load_acc<F8>(tacc + c * 32, v, sc);
       if (row_ok) {
         const int nv = min(32, p.H - col);
         if (p.accumulate) add_f32x32(dW + col, nv, v);
@@ -317,6 +351,40 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 
 // One stage of one CTA of the pair: its own 128 A rows, and its 128-row half of B (K-major:
 // one box; MN-major: two 64-wide chunks).
+// FP8: every operand is K-major (E4M3 copies, transposed where needed), one box each:
+//   FC1  A Xq [T][H]            B W1q [F][H] / [t][2][Fs][H]
+//   FC2  A Aq [T][t][Fs]        B W2q [t][H][Fs]             (K walks the shards)
+//   DGRAD A dYq [T][H]          B W2t [t][Fs][H]
+//   DX   A dZq [T][F1]          B W1t [H][F1]
+//   WGRAD_W2 A dYt [H][T]       B At [t][Fs][T]
+//   WGRAD_W1 A dZt [F1][T]      B Xt [H][T]
+template <GemmKind K>
+__device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUtensorMap* tB,
+                                               uint32_t sa, uint32_t sb, uint32_t bar, int mt,
+                                               int nt, int kb, int rank, const GemmParams& p) {
+  const int k0 = kb * kBK8;
+  const int nh = nt * kBN + 128 * rank;
+  if constexpr (K == GemmKind::FC1_GELU || K == GemmKind::DX || K == GemmKind::WGRAD_W1) {
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_2d(sb, tB, bar, k0, nh);
+  } else if constexpr (K == GemmKind::FC1_SWIGLU) {
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * 128;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_4d(sb, tB, bar, k0, j0, rank, i);
+  } else if constexpr (K == GemmKind::FC2) {
+    const int i = kb / p.kb_per_shard;
+    const int j0 = (kb - i * p.kb_per_shard) * kBK8;
+    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
+    tma_load_3d(sb, tB, bar, j0, nh, i);
+  } else {  // DGRAD_*, WGRAD_W2: B rows are shard i's rows j0.. of a [t][Fs][K] operand
+    const int i = nt / p.tiles_per_shard;
+    const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
+    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    tma_load_3d(sb, tB, bar, k0, j0, i);
+  }
+}
+
 template <GemmKind K>
 __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CUtensorMap* tB,
                                                  uint32_t sa, uint32_t sb, uint32_t bar, int mt,
@@ -362,7 +430,7 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
   }
 }
 
-template <GemmKind K>
+template <GemmKind K, bool F8 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -444,8 +512,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, kPairStageBytes);
-            issue_stage_pair<K>(&tmA, &tmB, sA0 + stage * kPairAStage, sB0 + stage * kPairBStage,
+            if constexpr (F8)
+              issue_stage_f8<K>(&tmA, &tmB, sA0 + stage * kPairAStage, sB0 + stage * kPairBStage,
                                 fb, mt, nt, kb, rank, p);
+            else
+              issue_stage_pair<K>(&tmA, &tmB, sA0 + stage * kPairAStage,
+                                  sB0 + stage * kPairBStage, fb, mt, nt, kb, rank, p);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
@@ -462,7 +534,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA issuer (pair)
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, KindOf<K>::a_mn, KindOf<K>::b_mn);
+      // FP8 reads every operand K-major; bf16 reads some MN-major (KindOf)
+      constexpr bool a_mn = !F8 && KindOf<K>::a_mn;
+      constexpr bool b_mn = !F8 && KindOf<K>::b_mn;
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(2 * kBM, kBN)
+                                    : idesc_bf16_f32(2 * kBM, kBN, a_mn, b_mn);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -482,13 +558,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = sA0 + stage * kPairAStage;
           const uint32_t sb = sB0 + stage * kPairBStage;
+          // four MMAs a stage: K = 16 bf16 or 32 E4M3 each, 32 bytes of every K-major row
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = KindOf<K>::a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
-                                                : sdesc(sa + kk * 32, 16, 1024, 2u);
-            const uint64_t bd = KindOf<K>::b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
-                                                : sdesc(sb + kk * 32, 16, 1024, 2u);
-            umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
+                                     : sdesc(sa + kk * 32, 16, 1024, 2u);
+            const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
+                                     : sdesc(sb + kk * 32, 16, 1024, 2u);
+            if constexpr (F8)
+              umma_f8_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair_mc(empty0 + 8 * stage, 0x3);
           if (++stage == S) {
@@ -525,6 +605,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    float sc = 1.0f;  // FP8: 2^-(k_a + k_b), exact
+    if constexpr (F8) sc = ldexpf(1.0f, -(e4m3_scale_exp(*p.amax_a) + e4m3_scale_exp(*p.amax_b)));
     int it = 0;
     for (int st = cid; st < num_super; st += nclusters, ++it) {
       const int buf = it & 1;
@@ -539,7 +621,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int mp, nt;
       tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
-      epilogue_tile<K>(tacc, row, mp * 2 + rank, nt, p);
+      float am = 0.0f;
+      epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am);
+      if constexpr (F8) {
+        if (p.amax_out != nullptr) {  // non-negative floats order like their bit patterns
+          const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(am));
+          if (lane == 0 && m != 0u) atomicMax(p.amax_out, m);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -48,6 +48,15 @@ struct GemmParams {
   uint64_t wait_ns;
   int fault_inject;
   int accumulate;  // weight-gradient kinds: add into the fp32 output instead of overwriting
+  // FP8 (E4M3) variants: the amax words of the two operands (their power-of-two scales
+  // are derived from them), and where FC1 / DGRAD record the amax of the bf16 A / dZ
+  // they write (the next GEMMs' operand)
+  const uint32_t* amax_a;
+  const uint32_t* amax_b;
+  uint32_t* amax_out;
 };
+
+// FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.
+constexpr int kBK8 = 128;
 
 }  // namespace mlpb

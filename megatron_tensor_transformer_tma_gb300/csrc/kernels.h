@@ -14,6 +14,10 @@ namespace mlpb {
 cudaError_t gemm_fwd_set_smem_attrs();
 cudaError_t gemm_bwd_set_smem_attrs();
 cudaError_t gemm_max_active_clusters(int* out);
+// gemm_fp8.cu: the same GEMMs on E4M3 operands (every operand K-major).
+cudaError_t gemm_f8_set_smem_attrs();
+cudaError_t launch_gemm_f8(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                           const GemmParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
@@ -43,5 +47,14 @@ cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, c
                           const float* dXn, const void* dres, float* dX, float* part_dg,
                           float* part_db, int64_t T, int64_t H, int shards, int blocks_per_shard,
                           uint32_t* err, uint64_t wait_ns, cudaStream_t s);
+
+// fp8.cu: *amax = max(*amax, max|in|) over n bf16 values (n % 8 == 0), as fp32 bits.
+cudaError_t launch_amax_bf16(const void* in, int64_t n, uint32_t* amax, int num_sms,
+                             cudaStream_t s);
+// fp8.cu: bf16 [batches][R][C] -> E4M3 codes q [batches][R][C] and/or qt [batches][C][R]
+// (either may be NULL) with the power-of-two scale of *amax; *k_out (if not NULL) gets
+// the scale exponent.  C % 8 == 0; R % 16 == 0 when qt is written.
+cudaError_t launch_cast_e4m3(const void* in, int batches, int64_t R, int64_t C, void* q,
+                             void* qt, const uint32_t* amax, int32_t* k_out, cudaStream_t s);
 
 }  // namespace mlpb

@@ -28,13 +28,14 @@ MLPB_ACT_SWIGLU = 1
 MLPB_FLAG_FAULT_INJECT = 0x1
 MLPB_FLAG_ACCUMULATE_GRADS = 0x2
 MLPB_FLAG_RECOMPUTE_ACT = 0x4
+MLPB_FLAG_FP8 = 0x8
 
 # Every symbol include/mlpb.h declares.
 EXPORTED = (
     "mlpb_create", "mlpb_destroy", "mlpb_workspace_size", "mlpb_saved_size", "mlpb_forward",
     "mlpb_backward", "mlpb_layernorm_sp_fwd", "mlpb_layernorm_sp_bwd", "mlpb_last_device_error",
     "mlpb_enable_timing", "mlpb_read_timings", "mlpb_status_str", "mlpb_bias_grad_noalloc",
-    "mlpb_branch_forward", "mlpb_branch_backward",
+    "mlpb_branch_forward", "mlpb_branch_backward", "mlpb_quantize_e4m3",
 )
 
 
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mlpb_bias_grad_noalloc": (I, [P, ctypes.c_int64, ctypes.c_int64, P, P]),
         "mlpb_branch_forward": (I, [H] + [P] * 15),
         "mlpb_branch_backward": (I, [H] + [P] * 19),
+        "mlpb_quantize_e4m3": (I, [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P,
+                                   P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -268,6 +271,25 @@ def mlpb_branch_backward(h: Handle, X, gamma, W1, W2, Xn, mean, rstd, Zsaved, As
     ]
     _check(load_library().mlpb_branch_backward(h.ptr, *args, _stream(stream)),
            "mlpb_branch_backward")
+
+
+def mlpb_quantize_e4m3(inp, q=None, qt=None, amax=None, scale_exp=None, stream=None):
+    """E4M3 codes (uint8 tensors) of a bf16 CUDA tensor [rows][cols] or [batches][rows][cols]
+    with one power-of-two scale; q in the input's layout, qt with the last two dimensions
+    swapped.  Returns (amax bits as an int32 CUDA tensor, scale exponent int32 CUDA tensor)."""
+    shape = tuple(inp.shape)
+    b, r, c = (1,) + shape if len(shape) == 2 else shape
+    dev = inp.device
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.int32, device=dev)
+    if scale_exp is None:
+        scale_exp = torch.empty(1, dtype=torch.int32, device=dev)
+    args = [_ptr(inp, torch.bfloat16, None, "in"), b, r, c,
+            _ptr(q, torch.uint8, shape, "q"),
+            _ptr(qt, torch.uint8, shape[:-2] + (c, r), "qt"),
+            _ptr(amax, torch.int32, (1,), "amax"), _ptr(scale_exp, torch.int32, (1,), "scale_exp")]
+    _check(load_library().mlpb_quantize_e4m3(*args, _stream(stream)), "mlpb_quantize_e4m3")
+    return amax, scale_exp
 
 
 def mlpb_last_device_error(h: Handle, stream=None) -> int:

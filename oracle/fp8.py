@@ -129,4 +129,24 @@ def mlp_backward_fp8(X, W1, b1, W2, dY, act="gelu"):
         dX = dZd @ _mlp.full_w1(W1d, act)
         dW1 = _mlp.shard_w1_grad(dZd.T @ Xd, t, act)
         db1 = dZ.sum(axis=0) if b1 is not None else None
-    return {"dX": dX, "dW1": dW1, "dW2": _mlp.shard_w2_grad(dW2f, t), "db1": db1, "db2": db2}
+    out = {"dX": dX, "dW1": dW1, "dW2": _mlp.shard_w2_grad(dW2f, t), "db1": db1, "db2": db2}
+    if act == "swiglu":
+        out.update(dG_bf16=dG, dU_bf16=dU)
+    else:
+        out["dZ_bf16"] = dZ
+    return out
+
+
+def block_fp8(X, gamma, beta, eps, W1, b1, W2, b2, dY, act):
+    """The pre-LN block with E4M3 GEMMs: LN (unchanged, Xn stored in bf16), the FP8 MLP on
+    Xn, and the LN backward of its input gradient."""
+    from . import layernorm as _ln
+    X = np.asarray(X, np.float64)
+    Xn, mu, rstd = _ln.layernorm_fwd(X, gamma, beta, eps)
+    Xn = round_bf16(Xn)
+    out = mlp_forward_fp8(Xn, W1, b1, W2, b2, act)
+    g = mlp_backward_fp8(Xn, W1, b1, W2, dY, act)
+    dX, dgamma, dbeta = _ln.layernorm_bwd(X, gamma, mu, rstd, g["dX"])
+    out.update(g)
+    out.update(Xn=Xn, dXn=g["dX"], dX=dX, dgamma=dgamma, dbeta=dbeta)
+    return out

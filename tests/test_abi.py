@@ -49,6 +49,8 @@ def test_status_strings(lib):
     (dict(hidden=0), mlpb.MLPB_EINVAL),
     (dict(tokens=-128), mlpb.MLPB_EINVAL),
     (dict(flags=0x80), mlpb.MLPB_EINVAL),
+    (dict(flags=mlpb.MLPB_FLAG_FP8, ffn=1040), mlpb.MLPB_EUNSUPPORTED),  # F/t % 16
+    (dict(flags=mlpb.MLPB_FLAG_FP8 | mlpb.MLPB_FLAG_RECOMPUTE_ACT), mlpb.MLPB_EUNSUPPORTED),
     (dict(seq_parallel_ln=True, ln_eps=0.0), mlpb.MLPB_EINVAL),
 ])
 def test_create_rejects_bad_configs(lib, kw, status):
@@ -66,7 +68,8 @@ def test_accumulate_flag_passes_config_validation(lib):
     for flags, ok in ((mlpb.MLPB_FLAG_ACCUMULATE_GRADS, True),
                       (mlpb.MLPB_FLAG_ACCUMULATE_GRADS | mlpb.MLPB_FLAG_FAULT_INJECT, True),
                       (mlpb.MLPB_FLAG_RECOMPUTE_ACT, True),
-                      (0x8, False)):
+                      (mlpb.MLPB_FLAG_FP8, True),
+                      (0x10, False)):
         cfg = mlpb.make_config(128, 256, 1024, 2, "gelu", True, flags=flags)
         h = ctypes.c_void_p()
         st = lib.mlpb_create(ctypes.byref(cfg), ctypes.byref(h))
@@ -80,7 +83,7 @@ def test_accumulate_flag_passes_config_validation(lib):
 def test_header_flag_values_match_binding():
     src = open(os.path.join(ROOT, "include", "mlpb.h")).read()
     for name in ("MLPB_FLAG_FAULT_INJECT", "MLPB_FLAG_ACCUMULATE_GRADS",
-                 "MLPB_FLAG_RECOMPUTE_ACT"):
+                 "MLPB_FLAG_RECOMPUTE_ACT", "MLPB_FLAG_FP8"):
         m = re.search(rf"#define\s+{name}\s+(0x[0-9a-fA-F]+)u", src)
         assert m and int(m.group(1), 16) == getattr(mlpb, name), name
 

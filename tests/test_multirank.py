@@ -39,7 +39,8 @@ def _run(rank, world, port):
     out = {"max": bench.reduce_max(1.5 + rank, torch.device("cpu"), world)}
     out["tflops"] = bench.job_tflops(2e12, world, 10.0)
     args = type("A", (), dict(workload=1, tp=None, tokens=None, warmup=0, steps=1,
-                              grad_accum=False, branch=False, recompute=False))()
+                              grad_accum=False, branch=False, recompute=False,
+                              fp8=False))()
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.run_reference(args, rank, world)
