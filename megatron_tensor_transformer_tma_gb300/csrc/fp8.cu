@@ -14,8 +14,8 @@ namespace mlpb {
 
 constexpr int kAmaxThreads = 256;
 constexpr int kAmaxBatch = 4;   // 16-byte loads in flight per thread
-constexpr int kCastRows = 64;   // tile rows (R)
-constexpr int kCastCols = 128;  // tile columns (C)
+constexpr int kCastRows = 64;   // CTA tile rows (R)
+constexpr int kCastCols = 256;  // CTA tile columns (C)
 constexpr int kCastThreads = 256;
 
 // *amax = max(*amax, max |in|) as fp32 bits.  |x| of a bf16 is its bits without the sign,
@@ -58,53 +58,68 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_bf16_kernel(const uint4* __
   }
 }
 
+// Transpose of an 8 x 8 byte block held as eight 8-byte rows: out[j] = column j.
+__device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                                             uint32_t& c0, uint32_t& c1, uint32_t& c2,
+                                             uint32_t& c3) {
+  const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r0, r1, 0x7362);
+  const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
+  c0 = __byte_perm(t0, t2, 0x5410);
+  c1 = __byte_perm(t0, t2, 0x7632);
+  c2 = __byte_perm(t1, t3, 0x5410);
+  c3 = __byte_perm(t1, t3, 0x7632);
+}
+
+__device__ __forceinline__ void transpose8x8(const uint2 (&row)[8], uint2 (&col)[8]) {
+  uint32_t a[4], b[4], c[4], d[4];
+  transpose4x4(row[0].x, row[1].x, row[2].x, row[3].x, a[0], a[1], a[2], a[3]);  // cols 0-3, rows 0-3
+  transpose4x4(row[4].x, row[5].x, row[6].x, row[7].x, b[0], b[1], b[2], b[3]);  // cols 0-3, rows 4-7
+  transpose4x4(row[0].y, row[1].y, row[2].y, row[3].y, c[0], c[1], c[2], c[3]);  // cols 4-7, rows 0-3
+  transpose4x4(row[4].y, row[5].y, row[6].y, row[7].y, d[0], d[1], d[2], d[3]);  // cols 4-7, rows 4-7
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    col[j] = make_uint2(a[j], b[j]);
+    col[4 + j] = make_uint2(c[j], d[j]);
+  }
+}
+
 // in bf16 [B][R][C] -> q e4m3 [B][R][C] (if kQ) and qt e4m3 [B][C][R] (if kQT), scale 2^k
-// from *amax.  A CTA converts a 64 x 128 tile: coalesced 16-byte reads along C, 8-byte
-// writes of q along C, and the transposed codes staged in shared memory for 16-byte
-// writes of qt along R.  Requires C % 8 == 0 and, for qt, R % 16 == 0.
+// from *amax.  Each thread converts an 8 x 8 block (eight 16-byte row loads), transposes
+// the codes in registers, and writes eight 8-byte rows of q and of qt.  A warp is 8 row
+// blocks x 4 column blocks (64 x 32 elements), so each load covers 64 contiguous bytes of
+// a row, each q store 32 bytes of a row and each qt store 64 bytes of a qt row; a CTA
+// stacks its 8 warps along C (64 x 256).  Requires R % 8 == 0 and C % 8 == 0.
 template <bool kQ, bool kQT>
 __global__ void __launch_bounds__(kCastThreads) cast_e4m3_kernel(
     const __nv_bfloat16* __restrict__ in, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
     const uint32_t* __restrict__ amax, int32_t* __restrict__ k_out, int64_t R, int64_t C) {
-  __shared__ __align__(16) uint8_t tile[kCastCols][kCastRows + 16];
   const int k = e4m3_scale_exp(*amax);
   if (k_out != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
       threadIdx.x == 0)
     *k_out = k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t r = static_cast<int64_t>(blockIdx.y) * kCastRows + (lane & 7) * 8;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * kCastCols + warp * 32 + (lane >> 3) * 8;
+  if (r >= R || c >= C) return;
   const int64_t plane = R * C;
-  in += blockIdx.z * plane;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kCastRows;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kCastCols;
-  const int cg = (threadIdx.x & 15) * 8;  // column offset of this thread's 8 values
+  const __nv_bfloat16* src = in + blockIdx.z * plane + r * C + c;
+  uint4 v[8];
 #pragma unroll
-  for (int pass = 0; pass < kCastRows / 16; ++pass) {
-    const int rl = (threadIdx.x >> 4) + 16 * pass;
-    const int64_t r = r0 + rl, c = c0 + cg;
-    if (r < R && c < C) {
-      const uint2 codes = e4m3x8_from_bf16x8(__ldg(reinterpret_cast<const uint4*>(in + r * C + c)),
-                                             k);
-      if constexpr (kQ)
-        *reinterpret_cast<uint2*>(q + blockIdx.z * plane + r * C + c) = codes;
-      if constexpr (kQT) {
+  for (int i = 0; i < 8; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src + i * C));
+  uint2 rows[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          tile[cg + e][rl] = static_cast<uint8_t>(codes.x >> (8 * e));
-          tile[cg + 4 + e][rl] = static_cast<uint8_t>(codes.y >> (8 * e));
-        }
-      }
-    }
+  for (int i = 0; i < 8; ++i) rows[i] = e4m3x8_from_bf16x8(v[i], k);
+  if constexpr (kQ) {
+    uint8_t* dst = q + blockIdx.z * plane + r * C + c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(dst + i * C) = rows[i];
   }
   if constexpr (kQT) {
-    __syncthreads();
+    uint2 cols[8];
+    transpose8x8(rows, cols);
+    uint8_t* dst = qt + blockIdx.z * plane + c * R + r;
 #pragma unroll
-    for (int pass = 0; pass < kCastCols / 64; ++pass) {
-      const int cl = (threadIdx.x >> 2) + 64 * pass;
-      const int rl = (threadIdx.x & 3) * 16;
-      const int64_t c = c0 + cl, r = r0 + rl;
-      if (c < C && r < R)
-        *reinterpret_cast<uint4*>(qt + blockIdx.z * plane + c * R + r) =
-            *reinterpret_cast<const uint4*>(&tile[cl][rl]);
-    }
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(dst + j * R) = cols[j];
   }
 }
 
@@ -144,7 +159,7 @@ extern "C" mlpb_status mlpb_quantize_e4m3(const void* in, int64_t batches, int64
                                           int32_t* scale_exp, mlpb_stream_t stream) {
   if (batches < 0 || rows < 0 || cols < 0) return MLPB_EINVAL;
   if (amax == nullptr || (q == nullptr && qt == nullptr)) return MLPB_EINVAL;
-  if (rows % 16 != 0 || cols % 16 != 0) return MLPB_EUNSUPPORTED;
+  if (rows % 16 != 0 || cols % 16 != 0) return MLPB_EUNSUPPORTED;  // (the kernels need 8)
   const int64_t n = batches * rows * cols;
   if (n > 0 && in == nullptr) return MLPB_EINVAL;
   for (const void* p : {in, static_cast<const void*>(q), static_cast<const void*>(qt)})

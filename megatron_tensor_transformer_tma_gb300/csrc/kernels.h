@@ -53,7 +53,7 @@ cudaError_t launch_amax_bf16(const void* in, int64_t n, uint32_t* amax, int num_
                              cudaStream_t s);
 // fp8.cu: bf16 [batches][R][C] -> E4M3 codes q [batches][R][C] and/or qt [batches][C][R]
 // (either may be NULL) with the power-of-two scale of *amax; *k_out (if not NULL) gets
-// the scale exponent.  C % 8 == 0; R % 16 == 0 when qt is written.
+// the scale exponent.  R % 8 == 0 and C % 8 == 0.
 cudaError_t launch_cast_e4m3(const void* in, int batches, int64_t R, int64_t C, void* q,
                              void* qt, const uint32_t* amax, int32_t* k_out, cudaStream_t s);
 
