@@ -85,10 +85,10 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&row)[8], uint2 (&col)
 
 // in bf16 [B][R][C] -> q e4m3 [B][R][C] (if kQ) and qt e4m3 [B][C][R] (if kQT), scale 2^k
 // from *amax.  Each thread converts an 8 x 8 block (eight 16-byte row loads), transposes
-// the codes in registers, and writes eight 8-byte rows of q and of qt.  A warp is 8 row
-// blocks x 4 column blocks (64 x 32 elements), so each load covers 64 contiguous bytes of
-// a row, each q store 32 bytes of a row and each qt store 64 bytes of a qt row; a CTA
-// stacks its 8 warps along C (64 x 256).  Requires R % 8 == 0 and C % 8 == 0.
+// the codes in registers, and writes eight 8-byte rows of q and of qt.  With qt a warp is
+// 8 row blocks x 4 column blocks (64 x 32 elements), so each load covers 64 contiguous
+// bytes of a row, each q store 32 bytes of a row and each qt store 64 bytes of a qt row;
+// a CTA stacks its 8 warps along C (64 x 256).  Requires R % 8 == 0 and C % 8 == 0.
 template <bool kQ, bool kQT>
 __global__ void __launch_bounds__(kCastThreads) cast_e4m3_kernel(
     const __nv_bfloat16* __restrict__ in, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
@@ -98,8 +98,12 @@ __global__ void __launch_bounds__(kCastThreads) cast_e4m3_kernel(
       threadIdx.x == 0)
     *k_out = k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t r = static_cast<int64_t>(blockIdx.y) * kCastRows + (lane & 7) * 8;
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * kCastCols + warp * 32 + (lane >> 3) * 8;
+  // with qt: a warp is 8 row blocks x 4 column blocks; without: 1 row block x 32 column
+  // blocks (512 contiguous bytes a load, 256 a store).  Either way a CTA covers 64 x 256.
+  const int rb = kQT ? (lane & 7) : warp;
+  const int cb = kQT ? warp * 4 + (lane >> 3) : lane;
+  const int64_t r = static_cast<int64_t>(blockIdx.y) * kCastRows + rb * 8;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * kCastCols + cb * 8;
   if (r >= R || c >= C) return;
   const int64_t plane = R * C;
   const __nv_bfloat16* src = in + blockIdx.z * plane + r * C + c;
