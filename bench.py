@@ -36,7 +36,8 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["gemm.cuh", "gemm_params.h", "ptx.cuh", "common.cuh", "gemm_fwd.cu",
-                  "gemm_bwd.cu", "reduce.cu", "layernorm.cu"]
+                  "gemm_bwd.cu", "gemm_fp8.cu", "fp8.cuh", "fp8.cu", "reduce.cu",
+                  "layernorm.cu"]
 
 
 def parse():
@@ -53,6 +54,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--branch", action="store_true",
                    help="the pre-norm MLP branch with its residual (SP-LN workloads)")
+    p.add_argument("--ncu-traffic", default=None, metavar="CSV",
+                   help="record the per-launch DRAM bytes of an ncu --csv capture "
+                        "(dram__bytes_read.sum, dram__bytes_write.sum) of this workload in "
+                        "profiles/traffic.json, for the current kernel sources, and exit")
     p.add_argument("--fp8", action="store_true",
                    help="E4M3 GEMM operands with per-tensor power-of-two scales")
     p.add_argument("--recompute", action="store_true",
@@ -463,6 +468,57 @@ def run_native(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+GEMM_KIND_NAMES = ["fc1_gelu", "fc1_swiglu", "fc2", "dgrad_gelu", "dgrad_swiglu", "dgrad_x",
+                   "wgrad_w2", "wgrad_w1"]
+
+
+def record_name(kernel_name):
+    """The bench record name of an ncu kernel name (gemm_pair_kernel<kind, fp8>), or None."""
+    import re
+    m = re.search(r"gemm_pair_kernel<(\d+), (\d+)>", kernel_name)
+    if not m:
+        return None
+    return GEMM_KIND_NAMES[int(m.group(1))] + ("_f8" if m.group(2) == "1" else "")
+
+
+def ingest_ncu_traffic(csv_path, wid):
+    """Average DRAM read + write bytes per launch of each GEMM in an ncu --csv capture,
+    merged into profiles/traffic.json under the current kernel-source hash."""
+    import csv
+    per = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 10]
+    head = rows[0]
+    ci = {k: head.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit",
+                                       "Metric Value")}
+    launches = {}
+    for r in rows[1:]:
+        name = record_name(r[ci["Kernel Name"]])
+        metric = r[ci["Metric Name"]]
+        if name is None or metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        assert r[ci["Metric Unit"]] == "byte", r[ci["Metric Unit"]]
+        v = float(r[ci["Metric Value"]].replace(",", ""))
+        launches.setdefault((r[ci["ID"]], name), {})[metric] = v
+    for (_, name), m in launches.items():
+        per.setdefault(name, []).append((m["dram__bytes_read.sum"], m["dram__bytes_write.sum"]))
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    recs = json.load(open(path)) if os.path.exists(path) else []
+    recs = [r for r in recs if not (r.get("workload") == wid and r.get("kernel") in per)]
+    h = kernel_source_hash()
+    for name, v in sorted(per.items()):
+        rd = sum(x for x, _ in v) / len(v)
+        wr = sum(y for _, y in v) / len(v)
+        recs.append({"kernel": name, "workload": wid, "source_hash": h,
+                     "dram_bytes_per_launch": rd + wr, "dram_read": rd, "dram_write": wr,
+                     "launches": len(v),
+                     "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                                "gpu__time_duration.sum (1 pass) on the full-size workload"})
+    with open(path, "w") as f:
+        json.dump(recs, f, indent=1)
+    return per
+
+
 def recorded_traffic(kernel, wid, shape):
     """DRAM bytes per launch from the committed ncu summary, if it is for this kernel,
     this workload and the current kernel sources; else None."""
@@ -545,6 +601,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world != args.gpus and "WORLD_SIZE" in os.environ:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.ncu_traffic:
+        per = ingest_ncu_traffic(args.ncu_traffic, args.workload)
+        print(json.dumps({k: len(v) for k, v in per.items()}))
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
