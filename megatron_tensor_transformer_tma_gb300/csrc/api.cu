@@ -477,7 +477,10 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
 // fc1 and fc2 of a validated forward; `resid` (bf16 [T][H] or NULL) is added to Y in
 // fc2's epilogue after b2.
 // The forward with E4M3 GEMMs: amax and E4M3 copies of X, W1, W2; fc1 (records amax(A));
-// the E4M3 copy of A; fc2.
+// the E4M3 copies of A and W2; fc2; all on the caller's stream, each GEMM's operands cast
+// right before it so that it finds them in L2.  (Running the weights' amax and casts on a
+// second stream beside X's and fc1 measured no faster: a persistent GEMM CTA holds 225 KB
+// of shared memory, so the casts cannot share its SMs.)
 static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, const void* b1,
                               const void* W2, const void* b2, float* Y, void* Zsaved,
                               void* Asaved, const void* resid, void* workspace, cudaStream_t s) {
@@ -485,19 +488,9 @@ static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, con
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
   const F8Layout L = f8_layout(h, workspace);
   uint32_t* am = L.amax;
-  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess) return MLPB_ECUDA;
-  mlpb_status st = f8_amax(h, X, T * H, am + kAmaxX, s, "fp8_amax_x");
-  if (st == MLPB_OK) st = f8_amax(h, W1, F1 * H, am + kAmaxW1, s, "fp8_amax_w1");
-  if (st == MLPB_OK) st = f8_amax(h, W2, F * H, am + kAmaxW2, s, "fp8_amax_w2");
-  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, L.Xq, nullptr, am + kAmaxX, s, "fp8_cast_x");
-  if (st == MLPB_OK)
-    st = f8_cast(h, W1, 1, F1, H, L.W1q, nullptr, am + kAmaxW1, s, "fp8_cast_w1");
-  if (st == MLPB_OK)
-    st = f8_cast(h, W2, 1, t * H, Fs, L.W2q, nullptr, am + kAmaxW2, s, "fp8_cast_w2");
-  if (st != MLPB_OK) return st;
 
-  // ---- fc1
-  CUtensorMap ta, tb;
+  // tensor maps first: an encoding error launches nothing
+  CUtensorMap ta1, tb1, ta2, tb2;
   GemmParams p = base_params(h);
   p.M = static_cast<int>(T);
   p.num_m_tiles = static_cast<int>(T / kBM);
@@ -507,35 +500,24 @@ static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, con
   p.amax_a = am + kAmaxX;
   p.amax_b = am + kAmaxW1;
   p.amax_out = am + kAmaxA;
-  p.fault_inject = h->fault_pending ? 1 : 0;
-  h->fault_pending = false;
-  if (!map_u8(&ta, L.Xq, H, T)) return MLPB_EINVAL;
+  bool ok = map_u8(&ta1, L.Xq, H, T);
   if (!h->swiglu) {
-    if (!map_u8(&tb, L.W1q, H, F)) return MLPB_EINVAL;
+    ok = ok && map_u8(&tb1, L.W1q, H, F);
     p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
     p.bias = static_cast<const __nv_bfloat16*>(b1);
-    st = run_gemm_f8(h, GemmKind::FC1_GELU, ta, tb, p, s, "fc1_gelu_f8", 2.0 * T * F * H,
-                     1.0 * (T * H + F * H) + 4.0 * T * F + (bias ? 2.0 * F : 0.0));
   } else {
     const uint64_t dims[4] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs), 2,
                               static_cast<uint64_t>(t)};
     const uint64_t str[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs * H),
                              static_cast<uint64_t>(2 * Fs * H)};
     const uint32_t box[4] = {128, 128, 1, 1};
-    if (!encode_u8(&tb, L.W1q, 4, dims, str, box)) return MLPB_EINVAL;
+    ok = ok && encode_u8(&tb1, L.W1q, 4, dims, str, box);
     p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
     p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
-    st = run_gemm_f8(h, GemmKind::FC1_SWIGLU, ta, tb, p, s, "fc1_swiglu_f8", 4.0 * T * F * H,
-                     1.0 * (T * H + 2 * F * H) + 6.0 * T * F);
   }
-  if (st == MLPB_OK)
-    st = f8_cast(h, Asaved, 1, T, F, L.Aq, nullptr, am + kAmaxA, s, "fp8_cast_a");
-  if (st != MLPB_OK) return st;
-
-  // ---- fc2 (the sum over shards accumulates in one TMEM tile; one scale for all shards)
-  if (!map_u8_sharded(&ta, L.Aq, Fs, T, t, F, Fs) ||
-      !map_u8_sharded(&tb, L.W2q, Fs, H, t, Fs, H * Fs))
-    return MLPB_EINVAL;
+  ok = ok && map_u8_sharded(&ta2, L.Aq, Fs, T, t, F, Fs) &&
+       map_u8_sharded(&tb2, L.W2q, Fs, H, t, Fs, H * Fs);
+  if (!ok) return MLPB_EINVAL;
   GemmParams q = base_params(h);
   q.M = static_cast<int>(T);
   q.num_m_tiles = static_cast<int>(T / kBM);
@@ -547,7 +529,31 @@ static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, con
   q.out0 = Y;
   q.amax_a = am + kAmaxA;
   q.amax_b = am + kAmaxW2;
-  return run_gemm_f8(h, GemmKind::FC2, ta, tb, q, s, "fc2_f8", 2.0 * T * H * F,
+
+  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess)
+    return MLPB_ECUDA;
+  mlpb_status st = f8_amax(h, W1, F1 * H, am + kAmaxW1, s, "fp8_amax_w1");
+  if (st == MLPB_OK) st = f8_amax(h, W2, F * H, am + kAmaxW2, s, "fp8_amax_w2");
+  if (st == MLPB_OK) st = f8_amax(h, X, T * H, am + kAmaxX, s, "fp8_amax_x");
+  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, L.Xq, nullptr, am + kAmaxX, s, "fp8_cast_x");
+  if (st == MLPB_OK)  // W1q last before fc1, so that fc1 finds it in L2
+    st = f8_cast(h, W1, 1, F1, H, L.W1q, nullptr, am + kAmaxW1, s, "fp8_cast_w1");
+  if (st == MLPB_OK) {
+    p.fault_inject = h->fault_pending ? 1 : 0;
+    h->fault_pending = false;
+    st = run_gemm_f8(h, h->swiglu ? GemmKind::FC1_SWIGLU : GemmKind::FC1_GELU, ta1, tb1, p, s,
+                     h->swiglu ? "fc1_swiglu_f8" : "fc1_gelu_f8",
+                     (h->swiglu ? 4.0 : 2.0) * T * F * H,
+                     h->swiglu ? 1.0 * (T * H + 2 * F * H) + 6.0 * T * F
+                               : 1.0 * (T * H + F * H) + 4.0 * T * F + (bias ? 2.0 * F : 0.0));
+  }
+  if (st == MLPB_OK)
+    st = f8_cast(h, Asaved, 1, T, F, L.Aq, nullptr, am + kAmaxA, s, "fp8_cast_a");
+  if (st == MLPB_OK)
+    st = f8_cast(h, W2, 1, t * H, Fs, L.W2q, nullptr, am + kAmaxW2, s, "fp8_cast_w2");
+  if (st != MLPB_OK) return st;
+  // ---- fc2 (the sum over shards accumulates in one TMEM tile; one scale for all shards)
+  return run_gemm_f8(h, GemmKind::FC2, ta2, tb2, q, s, "fc2_f8", 2.0 * T * H * F,
                      1.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
                          (resid ? 2.0 * T * H : 0.0));
 }
@@ -774,9 +780,13 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   return st;
 }
 
-// The backward with E4M3 GEMMs, on the caller's stream: amax of dY, W2, X, W1, A; E4M3
-// copies (dY both ways, W2 transposed); dgrad (records amax(dZ)); the bias sums; E4M3
-// copies of dZ (both ways), W1, X and A (transposed); dX, dW2, dW1.
+// The backward with E4M3 GEMMs, on the caller's stream.  Every amax first (they only
+// read); then each GEMM's E4M3 operands are written right before it, so that the GEMM
+// finds them in L2: dY (both ways) and W2 (transposed), dgrad (records amax(dZ)), db2;
+// dZ (both ways) and W1 (transposed), dX; A (transposed), dW2, db1; X (transposed), dW1.
+// (Casting beside the GEMMs on a second stream, like the bf16 backward's schedule,
+// measured 1-2 % slower: a persistent GEMM CTA holds 225 KB of shared memory, so the
+// casts cannot share its SMs.)
 static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, const void* W2,
                                const void* Zsaved, const void* Asaved, const void* dY,
                                float* dX, float* dW1, float* dW2, float* db1, float* db2,
@@ -791,22 +801,30 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
                                           align256(static_cast<size_t>(h->db2_splits) * H * 4));
   const F8Layout L = f8_layout(h, workspace);
   uint32_t* am = L.amax;
-  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess) return MLPB_ECUDA;
+
+  // tensor maps first: an encoding error launches nothing
+  CUtensorMap tdA, tdB, txA, txB, tw2A, tw2B, tw1A, tw1B;
+  if (!map_u8(&tdA, L.dYq, H, T) || !map_u8_sharded(&tdB, L.W2t, H, Fs, t, H, Fs * H) ||
+      !map_u8(&txA, L.dZq, F1, T) || !map_u8(&txB, L.W1t, F1, H) ||
+      !map_u8(&tw2A, L.dYt, T, H) || !map_u8_sharded(&tw2B, L.At, T, Fs, t, T, Fs * T) ||
+      !map_u8(&tw1A, L.dZt, T, F1) || !map_u8(&tw1B, L.Xt, T, H))
+    return MLPB_EINVAL;
+  if (cudaMemsetAsync(am, 0, kAmaxWords * sizeof(uint32_t), s) != cudaSuccess)
+    return MLPB_ECUDA;
+
   mlpb_status st = f8_amax(h, dY, T * H, am + kAmaxDY, s, "fp8_amax_dy");
   if (st == MLPB_OK) st = f8_amax(h, W2, F * H, am + kAmaxW2, s, "fp8_amax_w2");
   if (st == MLPB_OK) st = f8_amax(h, X, T * H, am + kAmaxX, s, "fp8_amax_x");
   if (st == MLPB_OK) st = f8_amax(h, W1, F1 * H, am + kAmaxW1, s, "fp8_amax_w1");
   if (st == MLPB_OK) st = f8_amax(h, Asaved, T * F, am + kAmaxA, s, "fp8_amax_a");
+
+  // ---- dgrad of fc2 with the fused activation derivative: dZ [T][F1] bf16
   if (st == MLPB_OK)
     st = f8_cast(h, dY, 1, T, H, L.dYq, L.dYt, am + kAmaxDY, s, "fp8_cast_dy");
   if (st == MLPB_OK)
     st = f8_cast(h, W2, static_cast<int>(t), H, Fs, nullptr, L.W2t, am + kAmaxW2, s,
                  "fp8_cast_w2t");
-  if (st != MLPB_OK) return st;
-  CUtensorMap ta, tb;
-
-  // ---- dgrad of fc2 with the fused activation derivative: dZ [T][F1] bf16
-  {
+  if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(T);
     p.num_m_tiles = static_cast<int>(T / kBM);
@@ -818,36 +836,22 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.amax_a = am + kAmaxDY;
     p.amax_b = am + kAmaxW2;
     p.amax_out = am + kAmaxDZ;
-    if (!map_u8(&ta, L.dYq, H, T) || !map_u8_sharded(&tb, L.W2t, H, Fs, t, H, Fs * H))
-      return MLPB_EINVAL;
-    st = run_gemm_f8(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, ta, tb, p, s,
-                     h->swiglu ? "dgrad_swiglu_f8" : "dgrad_gelu_f8", 2.0 * T * F * H,
+    st = run_gemm_f8(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, tdA, tdB,
+                     p, s, h->swiglu ? "dgrad_swiglu_f8" : "dgrad_gelu_f8", 2.0 * T * F * H,
                      1.0 * (T * H + F * H) + 4.0 * T * F1);
   }
-  // ---- bias sums on the bf16 dY and dZ
-  if (st == MLPB_OK && bias) {
+  if (st == MLPB_OK && bias) {  // db2 = sum_t dY on the bf16 dY
     LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H, 2);
     cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s, acc);
     lt.done();
     st = from_cuda(e);
-    if (st == MLPB_OK) {
-      LaunchTimer lt1(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
-      e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s, acc);
-      lt1.done();
-      st = from_cuda(e);
-    }
   }
+  // ---- dX = sum_i dZ_i W1_i (f backward: the K loop runs over every shard's rows)
   if (st == MLPB_OK)
     st = f8_cast(h, dZ, 1, T, F1, L.dZq, L.dZt, am + kAmaxDZ, s, "fp8_cast_dz");
   if (st == MLPB_OK)
     st = f8_cast(h, W1, 1, F1, H, nullptr, L.W1t, am + kAmaxW1, s, "fp8_cast_w1t");
-  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, nullptr, L.Xt, am + kAmaxX, s, "fp8_cast_xt");
-  if (st == MLPB_OK)
-    st = f8_cast(h, Asaved, 1, T, F, nullptr, L.At, am + kAmaxA, s, "fp8_cast_at");
-  if (st != MLPB_OK) return st;
-
-  // ---- dX = sum_i dZ_i W1_i (f backward: the K loop runs over every shard's rows)
-  {
+  if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(T);
     p.num_m_tiles = static_cast<int>(T / kBM);
@@ -856,11 +860,12 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.out0 = dX;
     p.amax_a = am + kAmaxDZ;
     p.amax_b = am + kAmaxW1;
-    if (!map_u8(&ta, L.dZq, F1, T) || !map_u8(&tb, L.W1t, F1, H)) return MLPB_EINVAL;
-    st = run_gemm_f8(h, GemmKind::DX, ta, tb, p, s, "dgrad_x_f8", 2.0 * T * H * F1,
+    st = run_gemm_f8(h, GemmKind::DX, txA, txB, p, s, "dgrad_x_f8", 2.0 * T * H * F1,
                      1.0 * (T * F1 + F1 * H) + 4.0 * T * H);
   }
   // ---- dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
+  if (st == MLPB_OK)
+    st = f8_cast(h, Asaved, 1, T, F, nullptr, L.At, am + kAmaxA, s, "fp8_cast_at");
   if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(H);
@@ -872,12 +877,17 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.accumulate = acc;
     p.amax_a = am + kAmaxDY;
     p.amax_b = am + kAmaxA;
-    if (!map_u8(&ta, L.dYt, T, H) || !map_u8_sharded(&tb, L.At, T, Fs, t, T, Fs * T))
-      return MLPB_EINVAL;
-    st = run_gemm_f8(h, GemmKind::WGRAD_W2, ta, tb, p, s, "wgrad_w2_f8", 2.0 * H * F * T,
+    st = run_gemm_f8(h, GemmKind::WGRAD_W2, tw2A, tw2B, p, s, "wgrad_w2_f8", 2.0 * H * F * T,
                      1.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
+  if (st == MLPB_OK && bias) {  // db1 = sum_t dZ on the bf16 dZ
+    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
+    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s, acc);
+    lt.done();
+    st = from_cuda(e);
+  }
   // ---- dW1 = dZ^T X  (M = F1, N = H, K = T)
+  if (st == MLPB_OK) st = f8_cast(h, X, 1, T, H, nullptr, L.Xt, am + kAmaxX, s, "fp8_cast_xt");
   if (st == MLPB_OK) {
     GemmParams p = base_params(h);
     p.M = static_cast<int>(F1);
@@ -888,8 +898,7 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.accumulate = acc;
     p.amax_a = am + kAmaxDZ;
     p.amax_b = am + kAmaxX;
-    if (!map_u8(&ta, L.dZt, T, F1) || !map_u8(&tb, L.Xt, T, H)) return MLPB_EINVAL;
-    st = run_gemm_f8(h, GemmKind::WGRAD_W1, ta, tb, p, s, "wgrad_w1_f8", 2.0 * F1 * H * T,
+    st = run_gemm_f8(h, GemmKind::WGRAD_W1, tw1A, tw1B, p, s, "wgrad_w1_f8", 2.0 * F1 * H * T,
                      1.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
   }
   return st;
