@@ -137,3 +137,34 @@ def test_branch_empty_batch_and_argument_errors():
     assert bool((Yb == 5.0).all())  # nothing ran
     assert mlpb.mlpb_last_device_error(br.handle) == 0
     br.close()
+
+
+def test_branch_with_recompute_and_accumulation_is_block_plus_residual_and_start():
+    """The residual branch with selective recomputation and gradient accumulation at once:
+    bit for bit the unfused block run with recomputation, plus the residual (Y + X,
+    dX + dY), with the parameter gradients added to seeded starting values."""
+    from inputs import make_main_grads
+    shape = MLPShape(384, 320, 1408, 4, "gelu", True, sp_ln=True)
+    d = make_inputs(shape, 75)
+    blk = run_gpu(shape, d, flags=mlpb.MLPB_FLAG_RECOMPUTE_ACT)
+    assert blk["status"] == 0
+    dev = torch.device("cuda:0")
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    br = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act, shape.bias,
+                        shape.ln_eps,
+                        flags=mlpb.MLPB_FLAG_RECOMPUTE_ACT | mlpb.MLPB_FLAG_ACCUMULATE_GRADS)
+    grads = br.alloc_grads(g["W1"], g["W2"])
+    names = ("dW1", "dW2", "db1", "db2", "dgamma", "dbeta")
+    main0 = make_main_grads({k: tuple(grads[k].shape) for k in names}, 75)
+    for k in names:
+        grads[k].copy_(main0[k])
+    Y = br.forward(g["X"], g["gamma"], g["beta"], g["W1"], g["b1"], g["W2"], g["b2"])
+    br.A.fill_(float("nan"))  # recomputation must not read the forward's A
+    br.backward(g["X"], g["gamma"], g["W1"], g["W2"], g["dY"], grads)
+    torch.cuda.synchronize()
+    assert mlpb.mlpb_last_device_error(br.handle) == 0
+    br.close()
+    assert torch.equal(Y, blk["Y"] + g["X"].float())
+    assert torch.equal(grads["dX"], blk["dX"] + g["dY"].float())
+    for k in names:
+        assert torch.equal(grads[k], main0[k].to(dev) + blk[k]), k

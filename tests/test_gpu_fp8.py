@@ -166,3 +166,47 @@ def test_fp8_full_size_within_format_error_of_bf16_path():
         assert torch.isfinite(v).all() and e < 0.12, (k, e)
         if k == "db2":  # the bias sum of dY does not pass through a GEMM
             assert torch.equal(v, ref)
+
+
+def test_fp8_bounded_wait_reports_timeout_and_context_survives():
+    """The fault-injection flag reaches the E4M3 GEMM too: its first launch's bounded wait
+    expires, the host reads MLPB_ETIMEOUT, and a fresh FP8 handle is correct afterwards."""
+    shape = MLPShape(128, 256, 1024, 2, "gelu", True)
+    d = make_inputs(shape, 96)
+    bad = run_gpu(shape, d, flags=FP8 | mlpb.MLPB_FLAG_FAULT_INJECT)
+    assert bad["status"] == mlpb.MLPB_ETIMEOUT
+    good = run_gpu(shape, d, flags=FP8)
+    assert good["status"] == 0
+    q, _ = _oracles(shape, d)
+    flips = _flip_bounds(shape, d, q)
+    for k in _names(shape):
+        gate_fp8(k, to_f64(good[k]), q[k], flips.get(k))
+
+
+def test_fp8_branch_with_accumulation_is_block_plus_residual_and_start():
+    """FP8 together with the residual branch and gradient accumulation: bit for bit the
+    FP8 block's outputs plus the residual (Y + X, dX + dY) and the parameter gradients
+    added to the buffers' seeded starting values (one fp32 add each)."""
+    from inputs import make_main_grads
+    shape = MLPShape(256, 384, 1024, 4, "swiglu", False, sp_ln=True)
+    d = make_inputs(shape, 97)
+    blk = run_gpu(shape, d, flags=FP8)
+    assert blk["status"] == 0
+    dev = torch.device("cuda:0")
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    br = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act, shape.bias,
+                        shape.ln_eps, flags=FP8 | mlpb.MLPB_FLAG_ACCUMULATE_GRADS)
+    grads = br.alloc_grads(g["W1"], g["W2"])
+    names = ("dW1", "dW2", "dgamma", "dbeta")
+    main0 = make_main_grads({k: tuple(grads[k].shape) for k in names}, 97)
+    for k in names:
+        grads[k].copy_(main0[k])
+    Y = br.forward(g["X"], g["gamma"], g["beta"], g["W1"], None, g["W2"], None)
+    br.backward(g["X"], g["gamma"], g["W1"], g["W2"], g["dY"], grads)
+    torch.cuda.synchronize()
+    assert mlpb.mlpb_last_device_error(br.handle) == 0
+    br.close()
+    assert torch.equal(Y, blk["Y"] + g["X"].float())
+    assert torch.equal(grads["dX"], blk["dX"] + g["dY"].float())
+    for k in names:
+        assert torch.equal(grads[k], main0[k].to(dev) + blk[k]), k
