@@ -50,7 +50,10 @@ def parse():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the token count (smaller cases for profiling)")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=40,
+                   help="timed end-to-end steps; the first step's uploads and the last "
+                        "step's downloads are not overlapped, so few steps understate "
+                        "the steady state")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--branch", action="store_true",
                    help="the pre-norm MLP branch with its residual (SP-LN workloads)")
