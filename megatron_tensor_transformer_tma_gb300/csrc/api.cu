@@ -688,20 +688,15 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   auto run_dw2 = [&]() -> mlpb_status {
     CUtensorMap ta, tb;
     GemmParams p = base_params(h);
-    p.M = static_cast<int>(H);
-    p.num_m_tiles = static_cast<int>(cdiv(H, kBM));
-    p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
-    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.M = static_cast<int>(F);
+    p.num_m_tiles = static_cast<int>(cdiv(F, kBM));
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW2;
     p.accumulate = acc;
-    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
-                               static_cast<uint64_t>(t)};
-    const uint64_t bstr[2] = {static_cast<uint64_t>(F * 2), static_cast<uint64_t>(Fs * 2)};
-    const uint32_t bbox[3] = {64, kBK, 1};
-    if (!map2d(&ta, dY, H, T, H, 64, kBK) || !encode_bf16(&tb, Asaved, 3, bdims, bstr, bbox))
+    if (!map2d(&ta, Asaved, F, T, F, 64, kBK) || !map2d(&tb, dY, H, T, H, 64, kBK))
       return MLPB_EINVAL;
-    return run_gemm(h, GemmKind::WGRAD_W2, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
+    return run_gemm(h, GemmKind::WGRAD_W2T, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
                     2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   };
   const bool recompute = h->recompute;

@@ -35,8 +35,8 @@ cudaError_t gemm_bwd_set_smem_attrs() {
   if (e == cudaSuccess) e = set_attr<GemmKind::DGRAD_GELU>();
   if (e == cudaSuccess) e = set_attr<GemmKind::DGRAD_SWIGLU>();
   if (e == cudaSuccess) e = set_attr<GemmKind::DX>();
-  if (e == cudaSuccess) e = set_attr<GemmKind::WGRAD_W2>();
   if (e == cudaSuccess) e = set_attr<GemmKind::WGRAD_W1>();
+  if (e == cudaSuccess) e = set_attr<GemmKind::WGRAD_W2T>();
   return e;
 }
 
@@ -49,10 +49,10 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
       return launch_one<GemmKind::DGRAD_SWIGLU>(a, b, p, clusters, s);
     case GemmKind::DX:
       return launch_one<GemmKind::DX>(a, b, p, clusters, s);
-    case GemmKind::WGRAD_W2:
-      return launch_one<GemmKind::WGRAD_W2>(a, b, p, clusters, s);
     case GemmKind::WGRAD_W1:
       return launch_one<GemmKind::WGRAD_W1>(a, b, p, clusters, s);
+    case GemmKind::WGRAD_W2T:
+      return launch_one<GemmKind::WGRAD_W2T>(a, b, p, clusters, s);
     default:
       return cudaErrorInvalidValue;
   }

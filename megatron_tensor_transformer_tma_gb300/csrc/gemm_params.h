@@ -15,6 +15,7 @@ enum class GemmKind : int {
   DX,
   WGRAD_W2,
   WGRAD_W1,
+  WGRAD_W2T,  // dW2 computed as its transpose: M = F, N = H (written into dW2's layout)
 };
 
 constexpr int kBM = 128;
