@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the token count (smaller cases for profiling)")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--e2e-copy-streams", type=int, default=2,
+                   help="copy streams per direction in the end-to-end leg")
     p.add_argument("--e2e-steps", type=int, default=40,
                    help="timed end-to-end steps; the first step's uploads and the last "
                         "step's downloads are not overlapped, so few steps understate "
@@ -471,8 +473,10 @@ def run_native(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# bench record names of the GEMM kinds, in the order of the library's GemmKind enum (the
+# bf16 dW2 is the transposed kind 8; kind 6 is its E4M3 form)
 GEMM_KIND_NAMES = ["fc1_gelu", "fc1_swiglu", "fc2", "dgrad_gelu", "dgrad_swiglu", "dgrad_x",
-                   "wgrad_w2", "wgrad_w1"]
+                   "wgrad_w2", "wgrad_w1", "wgrad_w2"]
 
 
 def record_name(kernel_name):
@@ -540,8 +544,10 @@ def recorded_traffic(kernel, wid, shape):
 def run_e2e(args, shape, d, step, new_outputs, results, out0, dev, world):
     """The same step through the binding with host buffers: every step copies all of its
     inputs from pinned host memory and reads all of its results back into pinned host
-    memory.  Copies run on their own streams into double-buffered device tensors, so the
-    transfers of neighbouring steps overlap this step's kernels."""
+    memory.  Copies run on their own streams (`--e2e-copy-streams` a direction, tensors
+    split between them by size so that several copy engines work at once) into
+    double-buffered device tensors, so the transfers of neighbouring steps overlap this
+    step's kernels."""
     import torch
     pinned = {k: (v.pin_memory() if v is not None else None) for k, v in d.items()}
     dev_in = [{k: (torch.empty_like(v, device=dev) if v is not None else None)
@@ -552,35 +558,55 @@ def run_e2e(args, shape, d, step, new_outputs, results, out0, dev, world):
     h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
     d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
     comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ns = max(1, args.e2e_copy_streams)
+
+    def split(sizes):
+        """Tensor names assigned to `ns` groups of about equal bytes (largest first)."""
+        groups, load = [[] for _ in range(ns)], [0] * ns
+        for k, n in sorted(sizes.items(), key=lambda kv: -kv[1]):
+            j = load.index(min(load))
+            groups[j].append(k)
+            load[j] += n
+        return groups
+
+    in_groups = split({k: v.numel() * v.element_size() for k, v in pinned.items()
+                       if v is not None})
+    out_groups = split({k: v.numel() * v.element_size() for k, v in host_out[0].items()})
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(ns)]
+    s_out = [torch.cuda.Stream(device=dev) for _ in range(ns)]
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    in_ready, in_free = [ev(), ev()], [ev(), ev()]
-    out_ready, out_free = [ev(), ev()], [ev(), ev()]
+    in_ready = [[ev() for _ in range(ns)] for _ in range(2)]
+    out_free = [[ev() for _ in range(ns)] for _ in range(2)]
+    in_free, out_ready = [ev(), ev()], [ev(), ev()]
     for b in range(2):
         in_free[b].record(comp)
-        out_free[b].record(comp)
+        for j in range(ns):
+            out_free[b][j].record(comp)
 
     def run(n):
         for i in range(n):
             b = i % 2
-            s_in.wait_event(in_free[b])
-            with torch.cuda.stream(s_in):
-                for k, v in pinned.items():
-                    if v is not None:
-                        dev_in[b][k].copy_(v, non_blocking=True)
-            in_ready[b].record(s_in)
-            comp.wait_event(in_ready[b])
-            comp.wait_event(out_free[b])
+            for j in range(ns):
+                s_in[j].wait_event(in_free[b])
+                with torch.cuda.stream(s_in[j]):
+                    for k in in_groups[j]:
+                        dev_in[b][k].copy_(pinned[k], non_blocking=True)
+                in_ready[b][j].record(s_in[j])
+                comp.wait_event(in_ready[b][j])
+                comp.wait_event(out_free[b][j])
             step(dev_in[b], outs[b])
             in_free[b].record(comp)
             out_ready[b].record(comp)
-            s_out.wait_event(out_ready[b])
-            with torch.cuda.stream(s_out):
-                for k, v in results(outs[b]).items():
-                    host_out[b][k].copy_(v, non_blocking=True)
-            out_free[b].record(s_out)
-        comp.wait_event(out_free[0])
-        comp.wait_event(out_free[1])
+            res = results(outs[b])
+            for j in range(ns):
+                s_out[j].wait_event(out_ready[b])
+                with torch.cuda.stream(s_out[j]):
+                    for k in out_groups[j]:
+                        host_out[b][k].copy_(res[k], non_blocking=True)
+                out_free[b][j].record(s_out[j])
+        for b in range(2):
+            for j in range(ns):
+                comp.wait_event(out_free[b][j])
 
     run(2)
     torch.cuda.synchronize()
@@ -594,7 +620,7 @@ def run_e2e(args, shape, d, step, new_outputs, results, out0, dev, world):
     return {"value": job_tflops(shape.gemm_flops(), world, ms), "unit": UNIT,
             "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "api": "mlpb_forward + mlpb_backward (+ SP-LN) via the ctypes binding",
-            "overlap": "H2D and D2H on their own streams, double-buffered device tensors"}
+            "overlap": f"H2D and D2H on {ns} streams each, double-buffered device tensors"}
 
 
 def main():

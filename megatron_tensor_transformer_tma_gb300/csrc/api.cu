@@ -566,39 +566,19 @@ static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, c
   const bool bias = h->cfg.has_bias != 0;
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t;
 
-  // ---- fc1 (column-parallel; f forward = every shard reads the same X)
-  CUtensorMap ta, tb;
-  GemmParams p = base_params(h);
-  p.M = static_cast<int>(T);
-  p.num_m_tiles = static_cast<int>(T / kBM);
-  p.num_kb = static_cast<int>(cdiv(H, kBK));
-  p.out0 = Zsaved;
-  p.out1 = Asaved;
-  p.fault_inject = h->fault_pending ? 1 : 0;
-  h->fault_pending = false;
-  if (!map2d(&ta, X, H, T, H, kBK, kBM)) return MLPB_EINVAL;
-  mlpb_status st;
+  // Tensor maps of both GEMMs first: an encoding error launches nothing.
+  CUtensorMap ta1, tb1, ta2, tb2;
+  bool ok = map2d(&ta1, X, H, T, H, kBK, kBM);
   if (!h->swiglu) {
-    if (!map2d(&tb, W1, H, F, H, kBK, kBN / 2)) return MLPB_EINVAL;
-    p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
-    p.bias = static_cast<const __nv_bfloat16*>(b1);
-    st = run_gemm(h, GemmKind::FC1_GELU, true, ta, tb, p, s, "fc1_gelu", 2.0 * T * F * H,
-                  2.0 * (T * H + F * H + 2 * T * F) + (bias ? 2.0 * F : 0.0));
+    ok = ok && map2d(&tb1, W1, H, F, H, kBK, kBN / 2);
   } else {
     const uint64_t dims[4] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Fs), 2,
                               static_cast<uint64_t>(t)};
     const uint64_t str[3] = {static_cast<uint64_t>(H * 2), static_cast<uint64_t>(Fs * H * 2),
                              static_cast<uint64_t>(2 * Fs * H * 2)};
     const uint32_t box[4] = {kBK, 128, 1, 1};
-    if (!encode_bf16(&tb, W1, 4, dims, str, box)) return MLPB_EINVAL;
-    p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
-    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
-    st = run_gemm(h, GemmKind::FC1_SWIGLU, true, ta, tb, p, s, "fc1_swiglu", 4.0 * T * F * H,
-                  2.0 * (T * H + 2 * F * H + 3 * T * F));
+    ok = ok && encode_bf16(&tb1, W1, 4, dims, str, box);
   }
-  if (st != MLPB_OK) return st;
-
-  // ---- fc2 (row-parallel; g forward = all t shards accumulate into one TMEM tile)
   {
     const uint64_t adims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(T),
                                static_cast<uint64_t>(t)};
@@ -608,22 +588,46 @@ static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, c
                                static_cast<uint64_t>(t)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
     const uint32_t bbox[3] = {kBK, kBN / 2, 1};
-    if (!encode_bf16(&ta, Asaved, 3, adims, astr, abox) ||
-        !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
-      return MLPB_EINVAL;
-    GemmParams q = base_params(h);
-    q.M = static_cast<int>(T);
-    q.num_m_tiles = static_cast<int>(T / kBM);
-    q.num_n_tiles = static_cast<int>(cdiv(H, kBN));
-    q.num_kb = static_cast<int>(t * q.kb_per_shard);
-    q.bias = static_cast<const __nv_bfloat16*>(b2);
-    q.aux = static_cast<const __nv_bfloat16*>(resid);
-    q.out0 = Y;
-    st = run_gemm(h, GemmKind::FC2, true, ta, tb, q, s, "fc2", 2.0 * T * H * F,
+    ok = ok && encode_bf16(&ta2, Asaved, 3, adims, astr, abox) &&
+         encode_bf16(&tb2, W2, 3, bdims, bstr, bbox);
+  }
+  if (!ok) return MLPB_EINVAL;
+
+  // ---- fc1 (column-parallel; f forward = every shard reads the same X)
+  GemmParams p = base_params(h);
+  p.M = static_cast<int>(T);
+  p.num_m_tiles = static_cast<int>(T / kBM);
+  p.num_kb = static_cast<int>(cdiv(H, kBK));
+  p.out0 = Zsaved;
+  p.out1 = Asaved;
+  p.fault_inject = h->fault_pending ? 1 : 0;
+  h->fault_pending = false;
+  mlpb_status st;
+  if (!h->swiglu) {
+    p.num_n_tiles = static_cast<int>(cdiv(F, kBN));
+    p.bias = static_cast<const __nv_bfloat16*>(b1);
+    st = run_gemm(h, GemmKind::FC1_GELU, true, ta1, tb1, p, s, "fc1_gelu", 2.0 * T * F * H,
+                  2.0 * (T * H + F * H + 2 * T * F) + (bias ? 2.0 * F : 0.0));
+  } else {
+    p.tiles_per_shard = static_cast<int>(cdiv(Fs, 128));
+    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    st = run_gemm(h, GemmKind::FC1_SWIGLU, true, ta1, tb1, p, s, "fc1_swiglu", 4.0 * T * F * H,
+                  2.0 * (T * H + 2 * F * H + 3 * T * F));
+  }
+  if (st != MLPB_OK) return st;
+
+  // ---- fc2 (row-parallel; g forward = all t shards accumulate into one TMEM tile)
+  GemmParams q = base_params(h);
+  q.M = static_cast<int>(T);
+  q.num_m_tiles = static_cast<int>(T / kBM);
+  q.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+  q.num_kb = static_cast<int>(t * q.kb_per_shard);
+  q.bias = static_cast<const __nv_bfloat16*>(b2);
+  q.aux = static_cast<const __nv_bfloat16*>(resid);
+  q.out0 = Y;
+  return run_gemm(h, GemmKind::FC2, true, ta2, tb2, q, s, "fc2", 2.0 * T * H * F,
                   2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
                       (resid ? 2.0 * T * H : 0.0));
-  }
-  return st;
 }
 
 mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const void* W2,
@@ -663,6 +667,22 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
   float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
                                           align256(static_cast<size_t>(h->db2_splits) * H * 4));
+  const bool recompute = h->recompute;
+
+  // Tensor maps of all four GEMMs first: an encoding error launches nothing.
+  CUtensorMap tdgA, tdgB, tw2A, tw2B, tw1A, tw1B, tdxA, tdxB;
+  {
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
+                               static_cast<uint64_t>(t)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
+    const uint32_t bbox[3] = {64, kBK, 1};
+    if (!map2d(&tdgA, dY, H, T, H, kBK, kBM) || !encode_bf16(&tdgB, W2, 3, bdims, bstr, bbox) ||
+        !map2d(&tw2A, Asaved, F, T, F, 64, kBK) || !map2d(&tw2B, dY, H, T, H, 64, kBK) ||
+        !map2d(&tw1A, dZ, F1, T, F1, 64, kBK) || !map2d(&tw1B, X, H, T, H, 64, kBK) ||
+        !map2d(&tdxA, dZ, F1, T, F1, kBK, kBM) || !map2d(&tdxB, W1, H, F1, H, 64, kBK))
+      return MLPB_EINVAL;
+  }
+
   // With per-kernel timing on, everything stays on `stream`, so that each kernel's
   // CUDA-event interval is its own and not shared with a concurrent one.
   cudaStream_t s2 = h->timing ? s : h->side;
@@ -671,7 +691,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
   if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
       cudaStreamWaitEvent(s2, h->ev_fork, 0) != cudaSuccess)
     return MLPB_ECUDA;
-  CUtensorMap ta, tb;
 
   // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
@@ -681,25 +700,6 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     lt.done();
     st = from_cuda(e);
   }
-
-  // ---- [s2] dW2_i = dY^T A_i  (M = H, N = F by shard, K = T), launched after dgrad (below):
-  // with recomputation the dgrad epilogue rewrites A first, and without it the same order
-  // (dW2 and dW1 beside dX, nothing beside dgrad) measured faster on the SwiGLU workloads.
-  auto run_dw2 = [&]() -> mlpb_status {
-    CUtensorMap ta, tb;
-    GemmParams p = base_params(h);
-    p.M = static_cast<int>(F);
-    p.num_m_tiles = static_cast<int>(cdiv(F, kBM));
-    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
-    p.num_kb = static_cast<int>(T / kBK);
-    p.out0 = dW2;
-    p.accumulate = acc;
-    if (!map2d(&ta, Asaved, F, T, F, 64, kBK) || !map2d(&tb, dY, H, T, H, 64, kBK))
-      return MLPB_EINVAL;
-    return run_gemm(h, GemmKind::WGRAD_W2T, false, ta, tb, p, s2, "wgrad_w2", 2.0 * H * F * T,
-                    2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
-  };
-  const bool recompute = h->recompute;
 
   // ---- [s] dgrad of fc2 with the fused activation derivative: dZ [T][F1]
   if (st == MLPB_OK) {
@@ -712,21 +712,28 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
     p.out0 = dZ;
     p.out1 = recompute ? Asaved : nullptr;
-    const uint64_t bdims[3] = {static_cast<uint64_t>(Fs), static_cast<uint64_t>(H),
-                               static_cast<uint64_t>(t)};
-    const uint64_t bstr[2] = {static_cast<uint64_t>(Fs * 2), static_cast<uint64_t>(H * Fs * 2)};
-    const uint32_t bbox[3] = {64, kBK, 1};
-    if (!map2d(&ta, dY, H, T, H, kBK, kBM) || !encode_bf16(&tb, W2, 3, bdims, bstr, bbox))
-      st = MLPB_EINVAL;
-    else
-      st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, ta, tb,
-                    p, s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H,
-                    2.0 * (T * H + F * H + 2 * T * F1) + (recompute ? 2.0 * T * F : 0.0));
+    st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, tdgA,
+                  tdgB, p, s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H,
+                  2.0 * (T * H + F * H + 2 * T * F1) + (recompute ? 2.0 * T * F : 0.0));
   }
   if (st == MLPB_OK && (cudaEventRecord(h->ev_dz, s) != cudaSuccess ||
                         cudaStreamWaitEvent(s2, h->ev_dz, 0) != cudaSuccess))
     st = MLPB_ECUDA;
-  if (st == MLPB_OK) st = run_dw2();
+
+  // ---- [s2] dW2_i^T = A_i^T dY  (M = F, N = H, K = T), written into dW2's layout; after
+  // dgrad: with recomputation its epilogue rewrites A first, and without it the same order
+  // (dW2 and dW1 beside dX, nothing beside dgrad) measured faster on the SwiGLU workloads
+  if (st == MLPB_OK) {
+    GemmParams p = base_params(h);
+    p.M = static_cast<int>(F);
+    p.num_m_tiles = static_cast<int>(cdiv(F, kBM));
+    p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
+    p.num_kb = static_cast<int>(T / kBK);
+    p.out0 = dW2;
+    p.accumulate = acc;
+    st = run_gemm(h, GemmKind::WGRAD_W2T, false, tw2A, tw2B, p, s2, "wgrad_w2", 2.0 * H * F * T,
+                  2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
+  }
 
   // ---- [s2] db1 = sum_t dZ
   if (st == MLPB_OK && bias) {
@@ -746,11 +753,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
     p.accumulate = acc;
-    if (!map2d(&ta, dZ, F1, T, F1, 64, kBK) || !map2d(&tb, X, H, T, H, 64, kBK))
-      st = MLPB_EINVAL;
-    else
-      st = run_gemm(h, GemmKind::WGRAD_W1, false, ta, tb, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
-                    2.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
+    st = run_gemm(h, GemmKind::WGRAD_W1, false, tw1A, tw1B, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
+                  2.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
   }
 
   // ---- [s] dX = sum_i dZ_i W1_i  (f backward: the sum over shards is the K loop)
@@ -761,11 +765,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
-    if (!map2d(&ta, dZ, F1, T, F1, kBK, kBM) || !map2d(&tb, W1, H, F1, H, 64, kBK))
-      st = MLPB_EINVAL;
-    else
-      st = run_gemm(h, GemmKind::DX, false, ta, tb, p, s, "dgrad_x", 2.0 * T * H * F1,
-                    2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+    st = run_gemm(h, GemmKind::DX, false, tdxA, tdxB, p, s, "dgrad_x", 2.0 * T * H * F1,
+                  2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
   }
 
   // Join: the caller's stream waits for s2 whatever happened above.
