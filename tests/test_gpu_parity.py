@@ -53,35 +53,43 @@ def test_deterministic_bitwise():
         assert torch.equal(a[k], b[k]), k
 
 
-def test_layernorm_sp_components():
-    """K8 / K9 alone on seeded inputs (the upstream dXn is seeded, not produced here)."""
-    shape = MLPShape(1024, 8192, 64, 8, "swiglu", False, sp_ln=True)
+@pytest.mark.parametrize("T,H,t", [
+    pytest.param(1024, 8192, 8, id="H8192-4-vectors-a-thread"),
+    pytest.param(512, 16384, 4, id="H16384-max-8-vectors"),
+    pytest.param(384, 12352, 3, id="H12352-8-vectors-ragged"),
+    pytest.param(256, 3072, 2, id="H3072-2-vectors"),
+    pytest.param(128, 64, 2, id="H64-min"),
+])
+def test_layernorm_sp_components(T, H, t):
+    """K8 / K9 alone on seeded inputs (the upstream dXn is seeded, not produced here), for
+    every register-block width the kernels instantiate (1, 2, 4, 8 vectors a thread)."""
+    shape = MLPShape(T, H, 8 * t, t, "swiglu", False, sp_ln=True)
     d = make_inputs(shape, 31)
     dXn = make_ln_grad(shape, 31)
     dev = torch.device("cuda:0")
-    h = mlpb.mlpb_create(mlpb.make_config(1024, 8192, 64, 8, "swiglu", False, True, 1e-5))
+    h = mlpb.mlpb_create(mlpb.make_config(T, H, 8 * t, t, "swiglu", False, True, 1e-5))
     X, gm, bt = d["X"].to(dev), d["gamma"].to(dev), d["beta"].to(dev)
     Xn = torch.empty_like(X)
-    mean = torch.empty(1024, device=dev)
-    rstd = torch.empty(1024, device=dev)
+    mean = torch.empty(T, device=dev)
+    rstd = torch.empty(T, device=dev)
     mlpb.mlpb_layernorm_sp_fwd(h, X, gm, bt, Xn, mean, rstd)
     ws = torch.empty(mlpb.mlpb_workspace_size(h), dtype=torch.uint8, device=dev)
-    dX = torch.empty((1024, 8192), device=dev)
-    dg = torch.empty(8192, device=dev)
-    db = torch.empty(8192, device=dev)
+    dX = torch.empty((T, H), device=dev)
+    dg = torch.empty(H, device=dev)
+    db = torch.empty(H, device=dev)
     mlpb.mlpb_layernorm_sp_bwd(h, X, gm, mean, rstd, dXn.to(dev), dX, dg, db, ws)
     torch.cuda.synchronize()
     assert mlpb.mlpb_last_device_error(h) == 0
     mlpb.mlpb_destroy(h)
     x64, g64, b64 = to_f64(d["X"]), to_f64(d["gamma"]), to_f64(d["beta"])
-    rXn, rmu, rrs = oln.layernorm_sp_fwd(x64, g64, b64, 1e-5, 8)
+    rXn, rmu, rrs = oln.layernorm_sp_fwd(x64, g64, b64, 1e-5, t)
     # Xn is bf16: within one bf16 rounding of the oracle plus 1e-3 RMS
     got = to_f64(Xn)
     assert np.all(np.abs(got - rXn) <= np.abs(rXn) * 2.0 ** -8 + 1e-3 * np.sqrt(np.mean(rXn ** 2)))
     # the mean is judged on the scale of the data it averages (rows have std ~1)
     assert np.abs(to_f64(mean) - rmu).max() <= 1e-5 * np.sqrt(np.mean(x64 ** 2))
     compare("rstd", to_f64(rstd), rrs, tol=1e-5)
-    rdX, rdg, rdb = oln.layernorm_sp_bwd(x64, g64, rmu, rrs, to_f64(dXn), 8)
+    rdX, rdg, rdb = oln.layernorm_sp_bwd(x64, g64, rmu, rrs, to_f64(dXn), t)
     compare("ln_dX", to_f64(dX), rdX, tol=1e-4)
     compare("dgamma", to_f64(dg), rdg, tol=1e-4)
     compare("dbeta", to_f64(db), rdb, tol=1e-4)
