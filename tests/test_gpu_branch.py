@@ -29,6 +29,10 @@ SMALL = [
     pytest.param(MLPShape(384, 320, 1408, 4, "gelu", True, sp_ln=True), 72,
                  id="gelu-t4-bias-raggedH-Fs352"),
     pytest.param(MLPShape(128, 128, 512, 2, "gelu", True, sp_ln=True), 73, id="gelu-t2-tiny"),
+    # the LayerNorm backward's residual variant at 2 and 8 vectors a thread
+    pytest.param(MLPShape(256, 3072, 512, 2, "gelu", True, sp_ln=True), 76, id="gelu-H3072"),
+    pytest.param(MLPShape(128, 16384, 256, 2, "swiglu", False, sp_ln=True), 77,
+                 id="swiglu-H16384"),
 ]
 
 

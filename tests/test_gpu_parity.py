@@ -53,6 +53,29 @@ def test_deterministic_bitwise():
         assert torch.equal(a[k], b[k]), k
 
 
+def test_timing_records_and_serialised_schedule_are_bitwise_equal():
+    """With per-kernel timing on, the backward runs on one stream: its outputs equal the
+    two-stream schedule's bit for bit, and every launch has a record with its algorithmic
+    flops and bytes."""
+    shape = MLPShape(256, 512, 2048, 4, "gelu", True)
+    d = make_inputs(shape, 22)
+    a = run_gpu(shape, d)
+    b = run_gpu(shape, d, timing=True)
+    assert a["status"] == 0 and b["status"] == 0
+    for k in ("Y", "dX", "dW1", "dW2", "db1", "db2", "Z", "A"):
+        assert torch.equal(a[k], b[k]), k
+    recs = b["timings"]
+    assert [r["name"] for r in recs] == ["fc1_gelu", "fc2", "colsum_db2", "dgrad_gelu",
+                                         "wgrad_w2", "colsum_db1", "wgrad_w1", "dgrad_x"]
+    T, H, F = shape.tokens, shape.hidden, shape.ffn
+    for r in recs:
+        assert r["ms"] > 0.0 and r["bytes"] > 0.0
+        if r["name"].startswith("colsum"):
+            assert r["flops"] == 0.0 and r["kernels"] == 2
+        else:
+            assert r["flops"] == 2.0 * T * H * F and r["kernels"] == 1
+
+
 @pytest.mark.parametrize("T,H,t", [
     pytest.param(1024, 8192, 8, id="H8192-4-vectors-a-thread"),
     pytest.param(512, 16384, 4, id="H16384-max-8-vectors"),
