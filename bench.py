@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None,
                    help="override the token count (smaller cases for profiling)")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--clocks-csv", default=None, metavar="PATH",
+                   help="keep the raw nvidia-smi samples of the timed region here")
     p.add_argument("--e2e-copy-streams", type=int, default=2,
                    help="copy streams per direction in the end-to-end leg")
     p.add_argument("--e2e-steps", type=int, default=40,
@@ -235,11 +237,17 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id):
+    def __init__(self, gpu_id, path=None):
+        """Samples nvidia-smi every 50 ms into `path` (a temporary file when None)."""
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        if path is None:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix="mlpb_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if os.path.dirname(self.path):
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
@@ -382,7 +390,7 @@ def run_native(args, rank, world, local_rank):
 
     # ---- timed region: inputs resident in HBM
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(gpu_smi_id(dev))
+    clocks = ClockSampler(gpu_smi_id(dev), args.clocks_csv)
     time.sleep(0.2)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
