@@ -158,7 +158,10 @@ mlpb_status mlpb_saved_size(const mlpb_handle *h, size_t *z_bytes, size_t *a_byt
  * shards with the fused bias+GELU or SwiGLU epilogue writes Zsaved and Asaved;
  * fc2 accumulates all t row shards into one accumulator per output tile (the
  * emulated g all-reduce) and adds b2 once, writing Y [T][H] fp32.  b1 and b2
- * must be NULL when has_bias is 0. */
+ * must be NULL when has_bias is 0.  `workspace` is NULL or mlpb_workspace_size() bytes:
+ * when given, fc2 uses it to split the K range of the tiles of its last, partly filled
+ * wave across idle SM pairs (their partial sums are added by a fixup kernel, in a fixed
+ * order); it is required under MLPB_FLAG_FP8. */
 mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const void *b1,
                          const void *W2, const void *b2, float *Y, void *Zsaved,
                          void *Asaved, void *workspace, mlpb_stream_t stream);

@@ -192,15 +192,31 @@ GemmParams base_params(const mlpb_handle* h) {
   return p;
 }
 
+// Tail split of a launch whose last wave of pair tiles is at most half full (FC2 and DX
+// with few, long-K tiles): the R tail tiles are cut into s = min(4, pairs / R) K-ranges
+// computed by different pairs, whose fp32 partials go to `partial` (at most one pair
+// tile a pair: max_clusters x 256 KB) and are summed by a fixup kernel.
+void plan_tail_split(const mlpb_handle* h, GemmParams& p, float* partial) {
+  const int super_tiles = static_cast<int>(cdiv(p.num_m_tiles, kClusterM)) * p.num_n_tiles;
+  const int clusters = std::min(super_tiles, h->max_clusters);
+  if (partial == nullptr || clusters <= 0) return;
+  const int tail = super_tiles % clusters;
+  if (tail == 0 || 2 * tail > clusters || p.num_kb < 2) return;
+  p.split = std::min(std::min(4, clusters / tail), p.num_kb);
+  p.split_start = super_tiles - tail;
+  p.partial = partial;
+}
+
 mlpb_status run_gemm(mlpb_handle* h, GemmKind kind, bool fwd, const CUtensorMap& a,
                      const CUtensorMap& b, const GemmParams& p, cudaStream_t s, const char* name,
                      double flops, double bytes) {
   const int super_tiles = static_cast<int>(cdiv(p.num_m_tiles, kClusterM)) * p.num_n_tiles;
   if (super_tiles == 0) return MLPB_OK;
   const int clusters = std::min(super_tiles, h->max_clusters);
-  LaunchTimer lt(h, s, name, flops, bytes);
+  LaunchTimer lt(h, s, name, flops, bytes, p.split > 1 ? 2 : 1);
   cudaError_t e = fwd ? launch_gemm_fwd(kind, a, b, p, clusters, s)
                       : launch_gemm_bwd(kind, a, b, p, clusters, s);
+  if (e == cudaSuccess && p.split > 1) e = launch_split_fixup(p, s);
   lt.done();
   return from_cuda(e);
 }
@@ -238,13 +254,28 @@ mlpb_status f8_cast(mlpb_handle* h, const void* x, int batches, int64_t R, int64
 
 size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
 
-size_t ws_backward_bytes(const mlpb_handle* h) {
+// Workspace of the bf16 path: dZ [T][F1] bf16, the bias sums' partials, then the tail
+// split's partial tiles (used by fc2 in the forward and by dX in the backward, beside the
+// bias sums on the other stream).
+size_t ws_split_offset(const mlpb_handle* h) {
   size_t b = ws_dz_bytes(h);
   if (h->cfg.has_bias) {
     b += align256(static_cast<size_t>(h->db2_splits) * h->H * 4);
     b += align256(static_cast<size_t>(h->db1_splits) * h->F * 4);
   }
   return b;
+}
+
+size_t ws_split_bytes(const mlpb_handle* h) {
+  return align256(static_cast<size_t>(h->max_clusters) * 2 * kBM * kBN * 4);
+}
+
+size_t ws_backward_bytes(const mlpb_handle* h) { return ws_split_offset(h) + ws_split_bytes(h); }
+
+float* ws_split_partial(const mlpb_handle* h, void* workspace) {
+  return workspace == nullptr
+             ? nullptr
+             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_split_offset(h));
 }
 
 size_t ws_ln_bytes(const mlpb_handle* h) {
@@ -625,6 +656,7 @@ static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, c
   q.bias = static_cast<const __nv_bfloat16*>(b2);
   q.aux = static_cast<const __nv_bfloat16*>(resid);
   q.out0 = Y;
+  plan_tail_split(h, q, ws_split_partial(h, workspace));
   return run_gemm(h, GemmKind::FC2, true, ta2, tb2, q, s, "fc2", 2.0 * T * H * F,
                   2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
                       (resid ? 2.0 * T * H : 0.0));
@@ -765,6 +797,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
+    plan_tail_split(h, p, ws_split_partial(h, workspace));
     st = run_gemm(h, GemmKind::DX, false, tdxA, tdxB, p, s, "dgrad_x", 2.0 * T * H * F1,
                   2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
   }

@@ -67,6 +67,24 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   nt = r / gm;
 }
 
+// Work unit u of a launch: a whole pair tile (part = -1) or, past split_start, one of the
+// `split` K-ranges of a tail tile.
+__device__ __forceinline__ void unit_range(int u, int split, int split_start, int num_kb, int& st,
+                                           int& kb0, int& kb1, int& part) {
+  if (u < split_start) {
+    st = u;
+    kb0 = 0;
+    kb1 = num_kb;
+    part = -1;
+    return;
+  }
+  const int j = u - split_start;
+  st = split_start + j / split;
+  part = j - (j / split) * split;
+  kb0 = num_kb * part / split;
+  kb1 = num_kb * (part + 1) / split;
+}
+
 // ------------------------------------------------------------------ pointwise math
 // tanh-form GELU written as z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), which is
 // the same function (1 + tanh(u) = 2 sigmoid(2u)) without cancellation for z << 0.
@@ -514,6 +532,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const WaitCtx wc{abort_flag, p.err, p.wait_ns};
   const int num_pm = (p.num_m_tiles + 1) / 2;
   const int num_super = num_pm * p.num_n_tiles;
+  const int split = p.split > 1 ? p.split : 1;
+  const int split_start = split > 1 ? p.split_start : num_super;
+  const int num_units = split_start + (num_super - split_start) * split;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -522,12 +543,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool skip_once = p.fault_inject != 0 && cid == 0 && leader;
-      for (int st = cid; st < num_super; st += nclusters) {
+      for (int u = cid; u < num_units; u += nclusters) {
+        int st, kb0, kb1, part;
+        unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
         int mp, nt;
         tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * 2 + rank;
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -567,14 +590,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int st = cid; st < num_super; st += nclusters, ++it) {
+      for (int u = cid; u < num_units; u += nclusters, ++it) {
+        int st, kb0, kb1, part;
+        unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
         const int buf = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
         if (!wait_bounded(tempty0 + 8 * buf, acc_par ^ 1u, wc, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull) ||
               !wait_bounded(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
             ok = false;
@@ -590,10 +615,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                      : sdesc(sa + kk * 32, 16, 1024, 2u);
             const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
                                      : sdesc(sb + kk * 32, 16, 1024, 2u);
+            const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
             if constexpr (F8)
-              umma_f8_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_f8_pair(d, ad, bd, idesc, accumulate);
             else
-              umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d, ad, bd, idesc, accumulate);
           }
           umma_commit_pair_mc(empty0 + 8 * stage, 0x3);
           if (++stage == S) {
@@ -610,9 +636,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------------------------------------------------------- relay (odd CTA)
       int stage = 0;
       uint32_t phase = 0;
-      for (int st = cid; st < num_super; st += nclusters) {
+      for (int u = cid; u < num_units; u += nclusters) {
+        int st, kb0, kb1, part;
+        unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteRelay)) {
             ok = false;
             break;
@@ -633,7 +661,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float sc = 1.0f;  // FP8: 2^-(k_a + k_b), exact
     if constexpr (F8) sc = ldexpf(1.0f, -(e4m3_scale_exp(*p.amax_a) + e4m3_scale_exp(*p.amax_b)));
     int it = 0;
-    for (int st = cid; st < num_super; st += nclusters, ++it) {
+    for (int u = cid; u < num_units; u += nclusters, ++it) {
+      int st, kb0, kb1, part;
+      unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
       const int buf = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       int ok = 1;
@@ -647,7 +677,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
       float am = 0.0f;
-      epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am);
+      if (part >= 0) {  // a K-range of a tail tile: raw partial sums, summed by the fixup
+        float* P = p.partial +
+                   ((static_cast<size_t>(st - split_start) * split + part) * 2 + rank) * (kBM * kBN) +
+                   static_cast<size_t>(row) * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          float v[32];
+          load_acc<F8>(tacc + c * 32, v, sc);
+          store_f32x32(P + c * 32, 32, v);
+        }
+      } else {
+        epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am);
+      }
       if constexpr (F8) {
         if (p.amax_out != nullptr) {  // non-negative floats order like their bit patterns
           const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(am));

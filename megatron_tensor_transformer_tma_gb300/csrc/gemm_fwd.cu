@@ -51,6 +51,66 @@ cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
   }
 }
 
+// Sums the tail tiles' partial K-ranges in part order and applies the fp32 epilogue of
+// FC2 / DX: Y[m][n] = ((sum_p P_p) + bias[n]) + resid[m][n] (bias, resid optional).  A CTA
+// covers 8 rows x 256 columns of one CTA half of one tile; a thread 8 columns.
+__global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
+  const int tiles_rows = kBM / 8;  // row groups a CTA half
+  const int j = blockIdx.x / (2 * tiles_rows);
+  const int rank = (blockIdx.x / tiles_rows) & 1;
+  const int r = (blockIdx.x % tiles_rows) * 8 + threadIdx.x / 32;
+  const int c = (threadIdx.x & 31) * 8;
+  const int num_pm = (p.num_m_tiles + 1) / 2;
+  int mp, nt;
+  tile_coords(p.split_start + j, num_pm, p.num_n_tiles, mp, nt);
+  const int m = (mp * 2 + rank) * kBM + r;
+  const int n = nt * kBN + c;
+  if (m >= p.M || n >= p.H) return;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int part = 0; part < p.split; ++part) {
+    const float* P = p.partial +
+                     ((static_cast<size_t>(j) * p.split + part) * 2 + rank) * (kBM * kBN) +
+                     static_cast<size_t>(r) * kBN + c;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(P));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(P + 4));
+    v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+    v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+  }
+  if (p.bias != nullptr) {
+    const uint4 u = ld_global_nc_v4(p.bias + n);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      v[2 * e] += f.x;
+      v[2 * e + 1] += f.y;
+    }
+  }
+  if (p.aux != nullptr) {
+    const uint4 u = ld_global_nc_v4(p.aux + static_cast<size_t>(m) * p.H + n);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      v[2 * e] += f.x;
+      v[2 * e + 1] += f.y;
+    }
+  }
+  float* Y = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H + n;
+  st_global_v4(Y, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                             __float_as_uint(v[3])));
+  st_global_v4(Y + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]),
+                                 __float_as_uint(v[6]), __float_as_uint(v[7])));
+}
+
+cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s) {
+  const int num_pm = (p.num_m_tiles + 1) / 2;
+  const int tail = num_pm * p.num_n_tiles - p.split_start;
+  if (p.split <= 1 || tail <= 0) return cudaSuccess;
+  split_fixup_kernel<<<tail * 2 * (kBM / 8), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 // Clusters of kClusterM GEMM CTAs that can be resident at once on this device.
 cudaError_t gemm_max_active_clusters(int* out) {
   cudaLaunchConfig_t cfg = {};

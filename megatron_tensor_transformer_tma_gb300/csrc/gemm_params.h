@@ -55,6 +55,13 @@ struct GemmParams {
   const uint32_t* amax_a;
   const uint32_t* amax_b;
   uint32_t* amax_out;
+  // Tail split: when split > 1, the tiles from super-tile `split_start` on (the last,
+  // partly filled wave) are each computed as `split` K-ranges by different pairs, which
+  // write raw fp32 partial tiles to `partial` ([tile][part][rank][128][256]); a fixup
+  // kernel sums them in part order and applies the epilogue.
+  int split;
+  int split_start;
+  float* partial;
 };
 
 // FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.

@@ -26,6 +26,8 @@ SMALL = [
     pytest.param(MLPShape(256, 256, 1024, 8, "gelu", True), 15, id="gelu-t8-Fs128"),
     pytest.param(MLPShape(256, 384, 1024, 4, "swiglu", False, sp_ln=True), 16, id="sp-ln-swiglu-t4"),
     pytest.param(MLPShape(128, 128, 512, 2, "gelu", True, sp_ln=True), 17, id="sp-ln-gelu-t2"),
+    # 80 pair tiles on 76 pairs: fc2 and dX split their 4 tail tiles' K range 4 ways
+    pytest.param(MLPShape(1024, 5120, 2048, 2, "gelu", True), 18, id="gelu-tail-split"),
 ]
 
 
