@@ -17,6 +17,11 @@
 // Every wait is bounded (common.cuh): a wait that expires raises the CTA's abort flag
 // and the device error word; all roles then drain what they issued and free TMEM.
 //
+// Pairs walk work units round robin: whole tiles, grouped 8 M-tile pairs at a time over
+// all N tiles, and -- when the host asks for a tail split (FC2, DX) -- the tiles of the
+// last, partly filled wave cut into K-ranges whose raw partial sums go to a workspace for
+// a fixup kernel (gemm_fwd.cu) to add up in a fixed order.
+//
 // The F8 instantiation runs the same pipeline on E4M3 operands (tcgen05 kind::f8f6f4, K = 32
 // a call, 128-byte = 128-element K-major rows, every operand K-major from its own or its
 // transposed E4M3 copy) and rescales each accumulator by 2^-(k_a + k_b) in the epilogue;
