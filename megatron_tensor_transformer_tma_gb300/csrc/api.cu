@@ -193,9 +193,10 @@ GemmParams base_params(const mlpb_handle* h) {
 }
 
 // Tail split of a launch whose last wave of pair tiles is at most half full (FC2 and DX
-// with few, long-K tiles): the R tail tiles are cut into s = min(4, pairs / R) K-ranges
-// computed by different pairs, whose fp32 partials go to `partial` (at most one pair
-// tile a pair: max_clusters x 256 KB) and are summed by a fixup kernel.
+// with few, long-K tiles; dW1, the backward's last GEMM): the R tail tiles are cut into
+// s = min(4, pairs / R) K-ranges computed by different pairs, whose fp32 partials go to
+// `partial` (at most one pair tile a pair: max_clusters x 256 KB) and are summed by a
+// fixup kernel.
 void plan_tail_split(const mlpb_handle* h, GemmParams& p, float* partial) {
   const int super_tiles = static_cast<int>(cdiv(p.num_m_tiles, kClusterM)) * p.num_n_tiles;
   const int clusters = std::min(super_tiles, h->max_clusters);
@@ -266,16 +267,21 @@ size_t ws_split_offset(const mlpb_handle* h) {
   return b;
 }
 
-size_t ws_split_bytes(const mlpb_handle* h) {
+// Two regions of at most one partial pair tile a pair: fc2 / dX use the first, dW1 (which
+// runs beside dX on the other stream) the second.
+size_t ws_split_region(const mlpb_handle* h) {
   return align256(static_cast<size_t>(h->max_clusters) * 2 * kBM * kBN * 4);
 }
 
+size_t ws_split_bytes(const mlpb_handle* h) { return 2 * ws_split_region(h); }
+
 size_t ws_backward_bytes(const mlpb_handle* h) { return ws_split_offset(h) + ws_split_bytes(h); }
 
-float* ws_split_partial(const mlpb_handle* h, void* workspace) {
+float* ws_split_partial(const mlpb_handle* h, void* workspace, int region = 0) {
   return workspace == nullptr
              ? nullptr
-             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_split_offset(h));
+             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_split_offset(h) +
+                                        region * ws_split_region(h));
 }
 
 size_t ws_ln_bytes(const mlpb_handle* h) {
@@ -785,6 +791,7 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
     p.accumulate = acc;
+    plan_tail_split(h, p, ws_split_partial(h, workspace, 1));  // the last GEMM of the step
     st = run_gemm(h, GemmKind::WGRAD_W1, false, tw1A, tw1B, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
                   2.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
   }

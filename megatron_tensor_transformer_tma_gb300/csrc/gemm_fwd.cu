@@ -52,7 +52,8 @@ cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
 }
 
 // Sums the tail tiles' partial K-ranges in part order and applies the fp32 epilogue of
-// FC2 / DX: Y[m][n] = ((sum_p P_p) + bias[n]) + resid[m][n] (bias, resid optional).  A CTA
+// FC2 / DX / WGRAD_W1: Y[m][n] = ((sum_p P_p) + bias[n]) + resid[m][n] (bias, resid
+// optional), or Y[m][n] += sum_p P_p when accumulating.  Y is [M][H] (dW1: M = F1).  A CTA
 // covers 8 rows x 256 columns of one CTA half of one tile; a thread 8 columns.
 __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
   const int tiles_rows = kBM / 8;  // row groups a CTA half
@@ -97,6 +98,12 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
     }
   }
   float* Y = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H + n;
+  if (p.accumulate) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(Y));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(Y + 4));
+    v[0] = a.x + v[0]; v[1] = a.y + v[1]; v[2] = a.z + v[2]; v[3] = a.w + v[3];
+    v[4] = b.x + v[4]; v[5] = b.y + v[5]; v[6] = b.z + v[6]; v[7] = b.w + v[7];
+  }
   st_global_v4(Y, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
                              __float_as_uint(v[3])));
   st_global_v4(Y + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]),

@@ -14,8 +14,9 @@ namespace mlpb {
 cudaError_t gemm_fwd_set_smem_attrs();
 cudaError_t gemm_bwd_set_smem_attrs();
 cudaError_t gemm_max_active_clusters(int* out);
-// gemm_fwd.cu: the fixup of a tail-split FC2 / DX launch (sums the partial K-ranges of
-// the tail tiles in part order, adds p.bias and p.aux when set, writes p.out0 fp32).
+// gemm_fwd.cu: the fixup of a tail-split FC2 / DX / WGRAD_W1 launch (sums the partial
+// K-ranges of the tail tiles in part order, adds p.bias and p.aux when set, writes or
+// with p.accumulate adds into p.out0, fp32 [M][H]).
 cudaError_t launch_split_fixup(const GemmParams& p, cudaStream_t s);
 // gemm_fp8.cu: the same GEMMs on E4M3 operands (every operand K-major).
 cudaError_t gemm_f8_set_smem_attrs();

@@ -30,6 +30,9 @@ SHAPES = [
     # SwiGLU behind the sequence-parallel LayerNorm: dgamma / dbeta accumulate too
     pytest.param(MLPShape(512, 384, 1024, 4, "swiglu", False, sp_ln=True), 52,
                  id="sp-ln-swiglu-t4"),
+    # micro-batches of 1024 tokens: dW1's 160 pair tiles end in a tail-split wave whose
+    # fixup adds into the buffers
+    pytest.param(MLPShape(2048, 5120, 2048, 2, "gelu", True), 54, id="gelu-tail-split"),
 ]
 
 
