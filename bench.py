@@ -19,6 +19,7 @@ exchange between GPUs on this path); `value` sums all ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -185,7 +186,14 @@ def bench_shape(args):
     shape = workload(args.workload, args.tp)
     if getattr(args, "branch", False) and not shape.sp_ln:
         raise SystemExit("--branch needs a workload with the sequence-parallel LayerNorm")
-    return shape if args.tokens is None else shape.with_tokens(args.tokens)
+    if args.tokens is None and args.tp is None:
+        return shape
+    if args.tokens is not None:
+        shape = shape.with_tokens(args.tokens)
+    # the workload's name carries its sizes: rename it after an override
+    kind = shape.name.split(" ")[0]
+    return dataclasses.replace(shape, name=f"{kind} T{shape.tokens} H{shape.hidden} "
+                                           f"F{shape.ffn} t{shape.tp}")
 
 
 def run_reference(args, rank, world):
@@ -455,7 +463,8 @@ def run_native(args, rank, world, local_rank):
         roofline = {"bound": "hbm", "kernel": top["name"], "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"{peak_src} copy"}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
-    roofline["traffic"] = recorded_traffic(top["name"], args.workload, shape)
+    plain = not (args.grad_accum or args.branch or args.recompute)
+    roofline["traffic"] = recorded_traffic(top["name"], args.workload, shape) if plain else None
 
     # ---- e2e: the same step from pinned host buffers, outputs read back every step
     e2e = run_e2e(args, shape, d, step, new_outputs, results, out, dev, world)
@@ -536,7 +545,11 @@ def ingest_ncu_traffic(csv_path, wid):
 
 def recorded_traffic(kernel, wid, shape):
     """DRAM bytes per launch from the committed ncu summary, if it is for this kernel,
-    this workload and the current kernel sources; else None."""
+    this workload at its own sizes and the current kernel sources; else None."""
+    from inputs import workload
+    ref = workload(wid)
+    if (shape.tokens, shape.tp) != (ref.tokens, ref.tp):
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
