@@ -145,8 +145,11 @@ mlpb_status mlpb_create(const mlpb_config *cfg, mlpb_handle **out);
 /* Frees the handle and its error word.  NULL is ignored. */
 void mlpb_destroy(mlpb_handle *h);
 
-/* Bytes of device scratch the caller passes as `workspace` to mlpb_backward and
- * mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16 and reduction partials). */
+/* Bytes of device scratch the caller passes as `workspace` to mlpb_forward,
+ * mlpb_backward and mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16, the column-sum
+ * partials, two regions of fp32 partial tiles for the K-range split of a GEMM's last
+ * wave -- dX and dW1 run at once on two streams -- and, under MLPB_FLAG_FP8, the
+ * E4M3 operand copies and their amax words). */
 mlpb_status mlpb_workspace_size(const mlpb_handle *h, size_t *bytes);
 
 /* Bytes of the saved activations: z_bytes for Z (GELU, T*F*2) or G|U (SwiGLU,
