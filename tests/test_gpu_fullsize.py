@@ -6,6 +6,8 @@ SwiGLU T8192/H8192/F28672/t8 blocks:
   * at full T, the outputs the oracle can compute one by one: 128 seeded token rows
     of Y and dX (rows 0, T-1 and every sequence shard's edges included), 64 seeded
     ffn features of dW1, dW2 and db1 (every shard seam included), and all of db2.
+    The last shard's seams lie in the last M tiles, which the tail split of fc2, dX and
+    dW1 cuts into K-ranges, so the sampled rows and features cross split tiles.
 """
 import numpy as np
 import pytest
