@@ -102,3 +102,11 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         mlpb.mlpb._ptr(torch.zeros(4), name="X")
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without libmlpb.so the binding raises: there is no other implementation to fall
+    back to."""
+    monkeypatch.setattr(mlpb.mlpb, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        mlpb.mlpb.load_library(str(tmp_path / "libmlpb.so"))
