@@ -274,25 +274,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 8:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    mx.append(float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[4:8]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+            return parse_clocks(f)
+
+
+def parse_clocks(lines):
+    """Median SM clock, maximum clock, sample count and the throttle reasons seen active,
+    from nvidia-smi lines of ClockSampler.FIELDS (csv, no header, no units); None when no
+    line parses."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[4:8]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
 
 
 def gpu_smi_id(dev):
