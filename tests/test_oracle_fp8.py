@@ -4,12 +4,18 @@
   spread over every binade, subnormals and ties included, and on the format itself:
   every one of the 254 finite codes is a fixed point, every midpoint between two
   neighbours goes to the one with an even code;
+* round_e4m3 against a table of values and codes that the format's definition in the
+  OCP 8-bit floating point specification fixes (tests/golden/e4m3_ofp8.txt: the extreme
+  normals and subnormals, ties to even in both directions, saturation), each code also
+  decoded here bit by bit and, below 480, converted by torch;
 * the scale exponent against its defining inequality;
 * a quantized GEMM against the same product formed from torch's E4M3 codes;
 * the FP8 block against the exact block within the error the format allows, and
   planted mistakes (truncation instead of rounding, a scale off by one power of two,
   a missing rescale) that the pins catch.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -35,6 +41,39 @@ def test_round_e4m3_matches_torch_conversion():
     x = np.concatenate([mags, -mags, r.uniform(-2 ** -6, 2 ** -6, 20000)])
     x = x[np.abs(x) <= 448.0].astype(np.float32).astype(np.float64)  # torch converts fp32
     assert np.array_equal(fp8.round_e4m3(x), _torch_e4m3(x))
+
+
+def _golden_e4m3():
+    """Rows (input, E4M3 value, code, torch agrees) of tests/golden/e4m3_ofp8.txt."""
+    def num(tok):
+        return float.fromhex(tok) if "x" in tok.lower() else float(tok)
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "e4m3_ofp8.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                a, v, c, t = line.split()
+                rows.append((num(a), num(v), int(c, 16), t == "1"))
+    return rows
+
+
+def _decode_e4m3(code):
+    """An E4M3 code's value from the bit fields: sign, exponent (bias 7), mantissa."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    return sign * (2.0 ** (e - 7) * (1 + m / 8) if e else 2.0 ** -6 * (m / 8))
+
+
+def test_round_e4m3_matches_the_format_table():
+    rows = _golden_e4m3()
+    assert len(rows) >= 20
+    x = np.array([r[0] for r in rows])
+    assert np.array_equal(fp8.round_e4m3(x), np.array([r[1] for r in rows]))
+    for a, v, code, torch_agrees in rows:
+        assert _decode_e4m3(code) == v, (a, hex(code))
+        if torch_agrees:
+            got = torch.tensor([a], dtype=torch.float32).to(torch.float8_e4m3fn) \
+                .view(torch.uint8).item()
+            assert got == code, (a, hex(got), hex(code))
 
 
 def test_round_e4m3_fixed_points_and_ties_to_even():
