@@ -18,7 +18,7 @@
 // and the device error word; all roles then drain what they issued and free TMEM.
 //
 // Pairs walk work units round robin: whole tiles, grouped 8 M-tile pairs at a time over
-// all N tiles, and -- when the host asks for a tail split (FC2, DX) -- the tiles of the
+// all N tiles, and -- when the host asks for a tail split (FC2, DX, WGRAD_W1) -- the tiles of the
 // last, partly filled wave cut into K-ranges whose raw partial sums go to a workspace for
 // a fixup kernel (gemm_fwd.cu) to add up in a fixed order.
 //
