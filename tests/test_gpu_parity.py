@@ -1,9 +1,9 @@
 """GPU parity of the C-ABI path against the fp64 oracle (element by element).
 
 Shapes span several 128 x 256 tiles and ragged tails: Fs not a multiple of 64 or 128
-(shard seams inside a K block and inside an N tile), H = 64 mod 128 (a ragged M tile in
-the dW2 GEMM and a ragged N tile in fc2 / dX), t = 1 and t = 8, with and without bias,
-GELU and SwiGLU, and the sequence-parallel pre-LN block.
+(shard seams inside a K block and inside an N tile), H = 64 mod 128 (a ragged N tile in
+fc2, dX, dW1 and dW2, which is computed as its transpose), t = 1 and t = 8, with and
+without bias, GELU and SwiGLU, and the sequence-parallel pre-LN block.
 """
 import numpy as np
 import pytest
