@@ -21,6 +21,7 @@ import pytest
 import torch
 
 from oracle import fp8
+from oracle import layernorm as oln
 from oracle import mlp
 
 
@@ -157,6 +158,31 @@ def test_fp8_block_within_format_error_of_exact_block(act, bias):
     if bias:  # db2 sees dY itself; db1 the bf16 dZ of the fp8 dgrad
         assert np.array_equal(f8["db2"], ex["db2"])
         assert _rms_rel(f8["db1"], ex["db1"]) < 0.12
+
+
+@pytest.mark.parametrize("act,bias", [("swiglu", False), ("gelu", True)])
+def test_fp8_pre_ln_block_within_format_error_and_wired_to_its_own_dxn(act, bias):
+    """block_fp8, the pre-LN block with E4M3 GEMMs, against the exact pre-LN block: every
+    output that passes through a GEMM within the format's error (above 0.5 % and under
+    12 % RMS, as for the MLP alone), Xn within one bf16 rounding (2^-8 relative) of the
+    exact LayerNorm output, and the LayerNorm backward applied to the block's own dXn: each row of dX
+    sums to zero, dbeta is the column sum of dXn."""
+    d = _inputs(64, 128, 256, 2, act, bias, 11)
+    r = np.random.default_rng(12)
+    gamma, beta, eps = 1 + 0.1 * r.standard_normal(128), 0.02 * r.standard_normal(128), 1e-5
+    f8 = fp8.block_fp8(d["X"], gamma, beta, eps, d["W1"], d["b1"], d["W2"], d["b2"], d["dY"],
+                       act)
+    ex = {**oln.block_forward(d["X"], gamma, beta, eps, d["W1"], d["b1"], d["W2"], d["b2"],
+                              act, 2),
+          **oln.block_backward(d["X"], gamma, beta, eps, d["W1"], d["b1"], d["W2"], d["dY"],
+                               act, 2)}
+    for k in ("Y", "dX", "dXn", "dW1", "dW2", "dgamma", "dbeta"):
+        e = _rms_rel(f8[k], ex[k])
+        assert 5e-3 < e < 0.12, (k, e)
+    assert np.all(np.abs(f8["Xn"] - ex["Xn"]) <= np.abs(ex["Xn"]) * 2.0 ** -8)  # bf16 u
+    scale = np.abs(f8["dX"]).max()
+    assert np.all(np.abs(f8["dX"].sum(axis=1)) <= 1e-12 * 128 * scale)
+    assert np.allclose(f8["dbeta"], f8["dXn"].sum(axis=0), rtol=1e-12, atol=0)
 
 
 def test_fp8_block_identity_on_exact_grid():
