@@ -98,6 +98,39 @@ def test_null_arguments(lib):
     lib.mlpb_destroy(None)
 
 
+def test_other_entry_points_reject_bad_arguments_before_the_device(lib):
+    """Null handles, null or misaligned pointers and unsupported sizes are refused on the
+    host; the pointers below are never dereferenced (validation returns first)."""
+    E, U = mlpb.MLPB_EINVAL, mlpb.MLPB_EUNSUPPORTED
+    assert lib.mlpb_branch_forward(None, *([None] * 15)) == E
+    assert lib.mlpb_branch_backward(None, *([None] * 19)) == E
+    assert lib.mlpb_enable_timing(None, 1) == E
+    count = ctypes.c_int()
+    assert lib.mlpb_read_timings(None, None, 0, ctypes.byref(count)) == E
+    assert lib.mlpb_last_device_error(None, None) == E
+    a, b = 0x10000, 0x20000  # 16-byte aligned stand-ins
+    # allocation-free column sum
+    assert lib.mlpb_bias_grad_noalloc(None, 64, 256, b, None) == E      # rows > 0, no input
+    assert lib.mlpb_bias_grad_noalloc(a, 64, 256, None, None) == E      # no output
+    assert lib.mlpb_bias_grad_noalloc(a, -1, 256, b, None) == E
+    assert lib.mlpb_bias_grad_noalloc(a, 64, 0, b, None) == E
+    assert lib.mlpb_bias_grad_noalloc(a, 64, 260, b, None) == U         # cols % 8
+    assert lib.mlpb_bias_grad_noalloc(a, 64, 1048576 + 8, b, None) == U  # beyond the scratch
+    assert lib.mlpb_bias_grad_noalloc(a + 4, 64, 256, b, None) == E     # misaligned input
+    assert lib.mlpb_bias_grad_noalloc(a, 64, 256, b + 8, None) == E     # misaligned output
+    # E4M3 quantization
+    q = lib.mlpb_quantize_e4m3
+    assert q(a, 1, 64, 64, b, None, None, None, None) == E          # no amax word
+    assert q(a, 1, 64, 64, None, None, b, None, None) == E          # neither q nor qt
+    assert q(a, -1, 64, 64, b, None, b, None, None) == E
+    assert q(a, 1, 72, 64, b, None, b, None, None) == U             # rows % 16
+    assert q(a, 1, 64, 40, b, None, b, None, None) == U             # cols % 16
+    assert q(None, 1, 64, 64, b, None, b, None, None) == E          # no input
+    assert q(a + 8, 1, 64, 64, b, None, b, None, None) == E         # misaligned input
+    assert q(a, 1, 64, 64, b, None, b + 2, None, None) == E         # misaligned amax
+    assert q(a, 65536, 16, 16, b, None, b, None, None) == U         # grid z limit
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
