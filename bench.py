@@ -72,8 +72,14 @@ def parse():
                    help="recompute the activation output in the backward (keep only Z)")
     p.add_argument("--grad-accum", action="store_true",
                    help="accumulate parameter gradients into fp32 main-grad buffers")
+    p.add_argument("--bf16-out", action="store_true",
+                   help="Y and dX (and the LayerNorm backward's dXn, dX) stored as bf16")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the extra block (the SwiGLU workloads' step and kernel rates, "
+                        "the LayerNorm kernels' bandwidth with a cold L2)")
+    p.add_argument("--extra-steps", type=int, default=8)
     return p.parse_args()
 
 
@@ -95,7 +101,8 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=False):
+def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=False,
+              bf16_out=False):
     return {"workload": (shape.name or f"workload {wid}") + (" + residual" if branch else ""),
             "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
@@ -103,6 +110,7 @@ def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=F
             "residual_branch": bool(branch), "grad_accum": bool(grad_accum),
             "recompute_act": bool(recompute),
             "gemm_operands": "e4m3 (per-tensor power-of-two scales)" if fp8 else "bf16",
+            "y_dx_dtype": "bf16" if bf16_out else "fp32",
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
@@ -312,6 +320,179 @@ def gpu_smi_id(dev):
     return dev.index or 0
 
 
+# ------------------------------------------------------------------ peaks and GPU identity
+PEAK_RULE = ("burst peak when the median SM clock sampled during the timed steps is at "
+             "least 0.95 of its maximum, else the sustained peak")
+
+
+def peak_regime(clk, peaks):
+    """("burst" | "sustained", dense bf16 TFLOP/s): the measured peak whose clock regime
+    the timed region ran in (PEAK_RULE); sustained when no clock was sampled."""
+    if clk and clk.get("sm_max_mhz") and clk["sm_mhz"] >= 0.95 * clk["sm_max_mhz"]:
+        return "burst", peaks["bf16_tflops"]
+    return "sustained", peaks["bf16_tflops_sustained"]
+
+
+def gpu_info(dev):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    drv = None
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                            "-i", str(dev.index or 0)], capture_output=True, text=True,
+                           timeout=20)
+        drv = r.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"name": props.name, "sms": props.multi_processor_count,
+            "cc": f"{props.major}.{props.minor}", "driver": drv,
+            "memory_gib": round(props.total_memory / 2 ** 30, 1),
+            "torch": torch.__version__, "cuda": torch.version.cuda}
+
+
+# ------------------------------------------------------------------ extra measurements
+def time_workload(wid, dev, steps, warmup):
+    """Median step time (CUDA events per step, inputs resident) and per-kernel rates of
+    one forward+backward of workload `wid` (with its LayerNorm when it has one)."""
+    import torch
+
+    import megatron_tensor_transformer_tma_gb300 as mlpb
+    from inputs import make_inputs, workload
+    shape = workload(wid)
+    d = make_inputs(shape, wid)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    del d
+    blk = mlpb.MLPBlock(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
+                        shape.bias, shape.sp_ln, shape.ln_eps)
+    T, H = shape.tokens, shape.hidden
+    o = {"Y": torch.empty((T, H), dtype=torch.float32, device=dev)}
+    o.update(blk.alloc_grads(g["W1"], g["W2"]))
+    if shape.sp_ln:
+        o["Xn"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        o["mean"] = torch.empty((T,), dtype=torch.float32, device=dev)
+        o["rstd"] = torch.empty((T,), dtype=torch.float32, device=dev)
+        o["dX_ln"] = torch.empty((T, H), dtype=torch.float32, device=dev)
+        o["dgamma"] = torch.empty((H,), dtype=torch.float32, device=dev)
+        o["dbeta"] = torch.empty((H,), dtype=torch.float32, device=dev)
+
+    def step():
+        X = g["X"]
+        if shape.sp_ln:
+            mlpb.mlpb_layernorm_sp_fwd(blk.handle, X, g["gamma"], g["beta"], o["Xn"], o["mean"],
+                                       o["rstd"])
+            X = o["Xn"]
+        blk.forward(X, g["W1"], g["b1"], g["W2"], g["b2"], o["Y"])
+        blk.backward(X, g["W1"], g["W2"], g["dY"], o)
+        if shape.sp_ln:
+            mlpb.mlpb_layernorm_sp_bwd(blk.handle, g["X"], g["gamma"], o["mean"], o["rstd"],
+                                       o["dX"], o["dX_ln"], o["dgamma"], o["dbeta"],
+                                       blk.workspace)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        step()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    ms = statistics.median(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    mlpb.mlpb_enable_timing(blk.handle, True)
+    kst = 2
+    for _ in range(kst):
+        step()
+    torch.cuda.synchronize()
+    recs = mlpb.mlpb_read_timings(blk.handle, capacity=64 * kst)
+    assert mlpb.mlpb_last_device_error(blk.handle) == 0, f"device error in workload {wid}"
+    blk.close()
+    per = {}
+    for r in recs:
+        k = per.setdefault(r["name"], [0.0, 0, r["flops"], r["bytes"]])
+        k[0] += r["ms"]
+        k[1] += 1
+    kernels = []
+    for name, (tot, n, fl, by) in sorted(per.items(), key=lambda kv: -kv[1][0]):
+        avg = tot / n
+        row = {"name": name, "avg_ms": round(avg, 4)}
+        if fl > 0:
+            row["tflops"] = round(fl / (avg * 1e-3) / 1e12, 1)
+        elif by > 0:
+            row["gbs"] = round(by / (avg * 1e-3) / 1e9, 1)
+        kernels.append(row)
+    return shape, ms, kernels
+
+
+def time_layernorm_cold(dev, T=8192, H=8192, t=8, iters=10):
+    """The LayerNorm forward and backward alone at T x H, each call timed on its own with
+    CUDA events after a 512 MB write that flushes L2 (so nothing starts in cache):
+    median GB/s of the algorithmic bytes (forward 4 B, backward 10 B an element)."""
+    import torch
+
+    import megatron_tensor_transformer_tma_gb300 as mlpb
+    from inputs import MLPShape, make_inputs, make_ln_grad
+    shape = MLPShape(T, H, 8 * t, t, "swiglu", False, sp_ln=True)
+    d = make_inputs(shape, 5)
+    h = mlpb.mlpb_create(mlpb.make_config(T, H, 8 * t, t, "swiglu", False, True, 1e-5))
+    X, gm, bt = d["X"].to(dev), d["gamma"].to(dev), d["beta"].to(dev)
+    dXn = make_ln_grad(shape, 5).to(dev)
+    Xn = torch.empty_like(X)
+    mean = torch.empty(T, device=dev)
+    rstd = torch.empty(T, device=dev)
+    dX = torch.empty((T, H), device=dev)
+    dg = torch.empty(H, device=dev)
+    db = torch.empty(H, device=dev)
+    ws = torch.empty(mlpb.mlpb_workspace_size(h), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        out = []
+        for i in range(iters + 2):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                out.append(e0.elapsed_time(e1))
+        return statistics.median(out)
+
+    fwd = timed(lambda: mlpb.mlpb_layernorm_sp_fwd(h, X, gm, bt, Xn, mean, rstd))
+    bwd = timed(lambda: mlpb.mlpb_layernorm_sp_bwd(h, X, gm, mean, rstd, dXn, dX, dg, db, ws))
+    assert mlpb.mlpb_last_device_error(h) == 0, "device error in the LayerNorm timing"
+    mlpb.mlpb_destroy(h)
+    n = T * H
+    fb, bb = 4.0 * n + 8.0 * T + 4.0 * H, 10.0 * n + 8.0 * T + 10.0 * H
+    return {"shape": f"T{T} H{H} t{t}", "l2": "flushed before every call (512 MB write)",
+            "ln_fwd_ms": round(fwd, 4), "ln_fwd_gbs": round(fb / (fwd * 1e-3) / 1e9, 1),
+            "ln_bwd_ms": round(bwd, 4), "ln_bwd_gbs": round(bb / (bwd * 1e-3) / 1e9, 1),
+            "note": "backward includes its dgamma/dbeta partial-sum pass"}
+
+
+def extra_measurements(args, dev, peaks, regime):
+    """The SwiGLU workloads' device throughput and kernel rates, and the LayerNorm
+    kernels' cold-cache bandwidth (the headline `value` stays the default workload)."""
+    import torch
+    bf16_peak = peaks["bf16_tflops"] if regime == "burst" else peaks["bf16_tflops_sustained"]
+    res = {"peak_regime": regime, "workloads": []}
+    for wid in (4, 5):
+        shape, ms, kernels = time_workload(wid, dev, max(3, args.extra_steps), 3)
+        tf = shape.gemm_flops() / (ms * 1e-3) / 1e12
+        res["workloads"].append({
+            "workload": shape.name, "ms_per_step": round(ms, 4), "tflops": round(tf, 1),
+            "frac_of_dense_bf16_peak": round(tf / bf16_peak, 4),
+            "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4),
+            "steps": max(3, args.extra_steps), "kernels": kernels})
+        torch.cuda.empty_cache()
+    ln = time_layernorm_cold(dev)
+    ln["ln_fwd_frac"] = round(ln["ln_fwd_gbs"] / peaks["hbm_gbs"], 4)
+    ln["ln_bwd_frac"] = round(ln["ln_bwd_gbs"] / peaks["hbm_gbs"], 4)
+    res["layernorm"] = ln
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ native leg
 def run_native(args, rank, world, local_rank):
     import torch
@@ -339,6 +520,8 @@ def run_native(args, rank, world, local_rank):
         flags |= mlpb.MLPB_FLAG_RECOMPUTE_ACT
     if args.fp8:
         flags |= mlpb.MLPB_FLAG_FP8
+    if args.bf16_out:
+        flags |= mlpb.MLPB_FLAG_BF16_OUT
     if args.branch:
         blk = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
                              shape.bias, shape.ln_eps, flags)
@@ -352,13 +535,14 @@ def run_native(args, rank, world, local_rank):
 
     def new_outputs():
         """Device buffers of one step's results (and the LN intermediates it needs)."""
-        o = {"Y": torch.empty((T, H), dtype=torch.float32, device=dev)}
+        out_dt = mlpb.out_dtype(blk.cfg)
+        o = {"Y": torch.empty((T, H), dtype=out_dt, device=dev)}
         o.update(blk.alloc_grads(g["W1"], g["W2"]))
         if shape.sp_ln and not args.branch:
             o["Xn"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
             o["mean"] = torch.empty((T,), dtype=torch.float32, device=dev)
             o["rstd"] = torch.empty((T,), dtype=torch.float32, device=dev)
-            o["dX_ln"] = torch.empty((T, H), dtype=torch.float32, device=dev)
+            o["dX_ln"] = torch.empty((T, H), dtype=out_dt, device=dev)
             o["dgamma"] = new_param((H,), dtype=torch.float32, device=dev)
             o["dbeta"] = new_param((H,), dtype=torch.float32, device=dev)
         return o
@@ -408,14 +592,15 @@ def run_native(args, rank, world, local_rank):
     clocks = ClockSampler(gpu_smi_id(dev), args.clocks_csv)
     time.sleep(0.2)
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
         step(g)
-    e1.record(stream)
+        evs[i + 1].record(stream)
     barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
+    ms_total = evs[0].elapsed_time(evs[-1])
+    ms_steps = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     assert mlpb.mlpb_last_device_error(h) == 0, "device error during the timed steps"
 
     # ---- per-kernel pass: the same steps with every launch bracketed by CUDA events on its
@@ -428,8 +613,8 @@ def run_native(args, rank, world, local_rank):
     recs = mlpb.mlpb_read_timings(h, capacity=64 * kernel_steps)
     mlpb.mlpb_enable_timing(h, False)
     kernel_step_launches = sum(r["kernels"] for r in recs) / kernel_steps
-    ms_total = reduce_max(ms_total, dev, world)
-    ms_step = ms_total / args.steps
+    ms_mean = reduce_max(ms_total / args.steps, dev, world)
+    ms_step = reduce_max(statistics.median(ms_steps), dev, world)
     value = job_tflops(shape.gemm_flops(), world, ms_step)
 
     # ---- per-kernel aggregation (CUDA events around each launch, same stream)
@@ -442,6 +627,7 @@ def run_native(args, rank, world, local_rank):
         k["kernels"] += r["kernels"]
     gpu_launches = int(round(kernel_step_launches * args.steps))
     peaks, peak_src = load_peaks()
+    regime, bf16_peak = peak_regime(clk, peaks)
     kernels = []
     for name, k in sorted(per.items(), key=lambda kv: -kv[1]["ms"]):
         avg = k["ms"] / k["launches"]
@@ -454,45 +640,59 @@ def run_native(args, rank, world, local_rank):
         kernels.append(row)
     top = kernels[0]
     topk = per[top["name"]]
-    if topk["flops"] > 0 and top["name"].endswith("_f8"):
+    if topk["flops"] > 0:
         achieved = topk["flops"] / (top["avg_ms"] * 1e-3) / 1e12
+        ratio = FP8_OVER_BF16 if top["name"].endswith("_f8") else 1.0
         roofline = {"bound": "tensor", "kernel": top["name"], "achieved": achieved,
-                    "peak": FP8_OVER_BF16 * peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "peak_source": f"{peak_src} sustained dense bf16 x {FP8_OVER_BF16} (nominal "
-                                   "dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)"}
-    elif topk["flops"] > 0:
-        achieved = topk["flops"] / (top["avg_ms"] * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": top["name"], "achieved": achieved,
-                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "peak_source": f"{peak_src} sustained dense bf16 (kernel timed inside a long step)"}
+                    "peak": ratio * bf16_peak, "unit": "TFLOP/s",
+                    "peak_source": f"{peak_src} {regime} dense bf16"
+                                   + (f" x {FP8_OVER_BF16} (nominal dense fp8 / bf16 ratio, "
+                                      "4.5 / 2.25 PFLOP/s)" if ratio != 1.0 else "")
+                                   + f" ({PEAK_RULE})",
+                    "frac_of_burst": achieved / (ratio * peaks["bf16_tflops"]),
+                    "frac_of_sustained": achieved / (ratio * peaks["bf16_tflops_sustained"])}
     else:
         achieved = topk["bytes"] / (top["avg_ms"] * 1e-3) / 1e9
         roofline = {"bound": "hbm", "kernel": top["name"], "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"{peak_src} copy"}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
-    plain = not (args.grad_accum or args.branch or args.recompute)
+    plain = not (args.grad_accum or args.branch or args.recompute or args.bf16_out)
     roofline["traffic"] = recorded_traffic(top["name"], args.workload, shape) if plain else None
 
     # ---- e2e: the same step from pinned host buffers, outputs read back every step
     e2e = run_e2e(args, shape, d, step, new_outputs, results, out, dev, world)
 
+    # ---- the other large workloads and the LayerNorm kernels, one line's worth each
+    extra = None
+    if rank == 0 and world == 1 and not args.no_extra:
+        blk.close()
+        del out, g
+        torch.cuda.empty_cache()
+        extra = extra_measurements(args, dev, peaks, regime)
+
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+               "ms_per_step_mean": ms_mean, "ms_per_step_stat": "median of the timed steps",
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "e4m3" if args.fp8 else "bf16",
                "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
                "config": config_of(shape, args.workload, args.grad_accum, args.branch,
-                               args.recompute, args.fp8),
-               "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
-               "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
+                                   args.recompute, args.fp8, args.bf16_out),
+               "frac_of_dense_bf16_peak": value / world / bf16_peak,
+               "frac_of_burst_peak": value / world / peaks["bf16_tflops"],
+               "frac_of_sustained_peak": value / world / peaks["bf16_tflops_sustained"],
+               "peak_tflops": bf16_peak, "peak_regime": regime,
+               "peak_source": f"{peak_src} ({PEAK_RULE})",
+               "gpu": gpu_info(dev),
                "roofline": roofline, "kernels": kernels,
                "kernel_timing": f"CUDA events around every launch over {kernel_steps} further "
                                 "steps, backward serialised on one stream",
                "gpu_launches": gpu_launches,
-               "e2e": e2e, "clocks": clk, "cpu_baseline": cpu}
+               "e2e": e2e, "clocks": clk, "cpu_baseline": cpu, "extra": extra}
         print(json.dumps(out), flush=True)
-    blk.close()
+    if extra is None:
+        blk.close()
     if world > 1:
         dist.destroy_process_group()
 

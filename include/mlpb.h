@@ -35,7 +35,7 @@
  *       Z saved (GELU)      [T][F]  bf16, column i*Fs+j = shard i, feature j
  *       Z saved (SwiGLU)    [T][t][2][Fs] bf16 (G then U of each shard)
  *       A saved             [T][F]  bf16
- *       Y, dX               [T][H] fp32
+ *       Y, dX               [T][H] fp32 (bf16 under MLPB_FLAG_BF16_OUT)
  *       dW1, dW2            fp32 in the layouts of W1, W2;  db1 [F], db2 [H] fp32
  *     where T = tokens, H = hidden, F = ffn, t = tp, Fs = F / t.
  *   - With T = 0 the per-row pointers (X, Y, Z/A saved, dY, dX, Xn, mean, rstd, dXn,
@@ -110,6 +110,28 @@ typedef enum { MLPB_ACT_GELU_TANH = 0, MLPB_ACT_SWIGLU = 1 } mlpb_act;
  * holds the E4M3 copies and is required by mlpb_forward too.  Requires F/tp % 16 == 0;
  * not combined with MLPB_FLAG_RECOMPUTE_ACT. */
 #define MLPB_FLAG_FP8 0x8u
+/* bf16 outputs (the mixed precision of the parallel linears in "The Tensor-Parallel
+ * Primitives": activations and their gradients travel in bf16).  With this flag Y
+ * (mlpb_forward, mlpb_branch_forward) and dX (mlpb_backward, mlpb_layernorm_sp_bwd,
+ * mlpb_branch_backward) are bf16 [T][H] instead of fp32, and mlpb_layernorm_sp_bwd reads
+ * its dXn as bf16 (what mlpb_backward then writes).  The sums are the same fp32 values
+ * as without the flag, rounded once to bf16 (nearest, ties to even) when stored; the
+ * parameter gradients stay fp32.  Halves those tensors' bytes, at the cost of one bf16
+ * rounding of Y and dX (up to 2^-9 of each value). */
+#define MLPB_FLAG_BF16_OUT 0x10u
+/* Emulated sequence-parallel exchange as copies (requires seq_parallel_ln; "The
+ * Tensor-Parallel Primitives": with sequence parallelism the linear layers all-gather the
+ * sequence-sharded activations in front of the column-parallel GEMM and reduce-scatter
+ * after the row-parallel one, and the conjugates in the backward).  Without the flag the
+ * gathered tensor is the row-block layout itself (shard s owns rows [s T/t, (s+1) T/t))
+ * and no byte moves.  With it, mlpb_forward first copies the input X into a gathered
+ * buffer in the workspace and writes fc2's output there before copying its rows out to Y
+ * (the scatter; the reduction over shards happened in the accumulator); mlpb_backward
+ * gathers X and dY and scatters dX the same way.  Results are bit for bit those of the
+ * view; the copies' bytes are reported apart from the algorithmic bytes (timing records
+ * "sp_gather_x", "sp_gather_dy", "sp_scatter_y", "sp_scatter_dx").  mlpb_forward then
+ * needs the workspace; the workspace holds 8*T*H more bytes. */
+#define MLPB_FLAG_EMULATE_COPIES 0x20u
 
 typedef struct {
   int64_t tokens;          /* T: rows of X; multiple of 128 (0 allowed)           */
@@ -146,8 +168,8 @@ mlpb_status mlpb_create(const mlpb_config *cfg, mlpb_handle **out);
 void mlpb_destroy(mlpb_handle *h);
 
 /* Bytes of device scratch the caller passes as `workspace` to mlpb_forward,
- * mlpb_backward and mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16, the column-sum
- * partials, two regions of fp32 partial tiles for the K-range split of a GEMM's last
+ * mlpb_backward and mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16, with a bias the
+ * db1 column sums of each 32-row group of dZ that the dgrad epilogue writes, two regions of fp32 partial tiles for the K-range split of a GEMM's last
  * wave -- dX and dW1 run at once on two streams -- and, under MLPB_FLAG_FP8, the
  * E4M3 operand copies and their amax words). */
 mlpb_status mlpb_workspace_size(const mlpb_handle *h, size_t *bytes);
@@ -166,12 +188,13 @@ mlpb_status mlpb_saved_size(const mlpb_handle *h, size_t *z_bytes, size_t *a_byt
  * wave across idle SM pairs (their partial sums are added by a fixup kernel, in a fixed
  * order); it is required under MLPB_FLAG_FP8. */
 mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const void *b1,
-                         const void *W2, const void *b2, float *Y, void *Zsaved,
+                         const void *W2, const void *b2, void *Y, void *Zsaved,
                          void *Asaved, void *workspace, mlpb_stream_t stream);
 
 /* Backward of the block for an upstream gradient dY [T][H] bf16.  g backward is
  * the identity (every shard reads the same dY); dZ = (dY W2_i) * act'(.) per
- * shard; dW2_i = dY^T A_i; dW1_i = dZ_i^T X; db1 = sum_t dZ; db2 = sum_t dY;
+ * shard; dW2_i = dY^T A_i; dW1_i = dZ_i^T X; db1 = sum_t dZ (column sums of the bf16
+ * dZ taken in the dgrad epilogue, then added in row order); db2 = sum_t dY (one launch);
  * dX = sum_i dZ_i W1_i with the sum over shards accumulated in one tensor-memory
  * accumulator (the emulated f all-reduce).  db1/db2 must be NULL without bias.
  * `workspace` must hold mlpb_workspace_size() bytes.  Asaved is read only (the
@@ -179,7 +202,7 @@ mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const vo
  * backward writes before reading. */
 mlpb_status mlpb_backward(mlpb_handle *h, const void *X, const void *W1, const void *W2,
                           const void *Zsaved, void *Asaved, const void *dY,
-                          float *dX, float *dW1, float *dW2, float *db1, float *db2,
+                          void *dX, float *dW1, float *dW2, float *db1, float *db2,
                           void *workspace, mlpb_stream_t stream);
 
 /* Sequence-parallel LayerNorm forward ("The Tensor-Parallel Primitives": norms
@@ -194,25 +217,27 @@ mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle *h, const void *X, const void *gam
                                   mlpb_stream_t stream);
 
 /* Sequence-parallel LayerNorm backward for dXn [T][H] fp32 (the dX output of
- * mlpb_backward run on Xn).  dX [T][H] fp32; dgamma, dbeta [H] fp32 are the sum
+ * mlpb_backward run on Xn; bf16 under MLPB_FLAG_BF16_OUT).  dX [T][H] fp32 (bf16 under
+ * MLPB_FLAG_BF16_OUT; it may be the dXn buffer itself); dgamma, dbeta [H] fp32 are the sum
  * over shards of each shard's partials (the all-reduce the SP layout implies).
  * `workspace` must hold mlpb_workspace_size() bytes. */
 mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle *h, const void *X, const void *gamma,
-                                  const float *mean, const float *rstd, const float *dXn,
-                                  float *dX, float *dgamma, float *dbeta, void *workspace,
+                                  const float *mean, const float *rstd, const void *dXn,
+                                  void *dX, float *dgamma, float *dbeta, void *workspace,
                                   mlpb_stream_t stream);
 
 /* Pre-norm MLP branch of a transformer layer ("The Transformer Stack": the layer runs
  * its MLP branch on the layer-normalised input and adds the branch input back through a
  * residual connection; dropout is left out), sequence-parallel:
- *     Y = X + MLP(LN(X))        (Y [T][H] fp32; X, gamma, beta bf16)
+ *     Y = X + MLP(LN(X))        (Y [T][H] fp32, bf16 under MLPB_FLAG_BF16_OUT; X, gamma,
+ *                                beta bf16)
  * Runs mlpb_layernorm_sp_fwd (writes Xn, mean, rstd, kept for the backward) and the
  * forward of mlpb_forward on Xn, with X added to every output element in fc2's epilogue
  * after b2 (the residual of a row lives on the sequence shard that owns the row).
  * Requires seq_parallel_ln.  Arguments as in the two calls it combines. */
 mlpb_status mlpb_branch_forward(mlpb_handle *h, const void *X, const void *gamma,
                                 const void *beta, const void *W1, const void *b1,
-                                const void *W2, const void *b2, float *Y, void *Xn,
+                                const void *W2, const void *b2, void *Y, void *Xn,
                                 float *mean, float *rstd, void *Zsaved, void *Asaved,
                                 void *workspace, mlpb_stream_t stream);
 
@@ -226,7 +251,7 @@ mlpb_status mlpb_branch_forward(mlpb_handle *h, const void *X, const void *gamma
 mlpb_status mlpb_branch_backward(mlpb_handle *h, const void *X, const void *gamma,
                                  const void *W1, const void *W2, const void *Xn,
                                  const float *mean, const float *rstd, const void *Zsaved,
-                                 void *Asaved, const void *dY, float *dX, float *dW1,
+                                 void *Asaved, const void *dY, void *dX, float *dW1,
                                  float *dW2, float *db1, float *db2, float *dgamma,
                                  float *dbeta, void *workspace, mlpb_stream_t stream);
 
@@ -251,10 +276,13 @@ mlpb_status mlpb_read_timings(mlpb_handle *h, mlpb_kernel_time *out, int capacit
  * The pages have no counterpart: this is an allocation-free variant of the same kernels.
  * It needs no handle and no workspace: its scratch is a fixed 4 MiB device array inside
  * the library (held by every GPU that loads the library until the process exits).
- * The first call on a device looks up that array's device address and the SM count
- * (once per device, with the device current); make that first call before any stream
- * capture.  Every call shares the one array: calls whose kernels overlap on the GPU
- * (other streams, other host threads) race on it and must be serialised by the caller.
+ * Each call looks up that array's device address on the current device (a host-side
+ * lookup, so a device reset or a re-created context cannot leave a stale address); the
+ * first call on a device also loads the library's device code there, so make it before
+ * any stream capture.  Every call shares the one array and the array keeps the last
+ * call's partial sums; each call writes every partial it reads before reading it, so
+ * nothing needs clearing.  Calls whose kernels overlap on the GPU (other streams, other
+ * host threads) race on the array and must be serialised by the caller.
  * Requires cols % 8 == 0 and cols <= 1048576 (one split of fp32 partials must fit the
  * scratch; larger widths return MLPB_EUNSUPPORTED), 16-byte aligned `in` and `out`;
  * rows may be 0 (out becomes zeros, `in` may then be NULL).  Allocates nothing. */

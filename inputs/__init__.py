@@ -15,4 +15,8 @@ from .mlp_inputs import (  # noqa: F401
     sample_rows,
     sample_ffn_cols,
     reduced_tokens,
+    make_saturating_inputs,
+    make_zero_block_inputs,
+    make_ln_edge_rows,
+    LN_EDGE_KINDS,
 )

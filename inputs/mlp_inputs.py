@@ -170,3 +170,57 @@ def sample_ffn_cols(shape: MLPShape, wid: int, n: int = 64) -> torch.Tensor:
     perm = torch.randperm(F, generator=_gen(wid, "cols"))[:n].tolist()
     cols = sorted(must | set(perm[: max(0, n - len(must))]))
     return torch.tensor(cols, dtype=torch.int64)
+
+
+# ---------------------------------------------------------------- edge cases
+# Seeds of the edge-case draws: SEED_BASE + 1000 * wid + 500 + k (k as in _K), apart from
+# the workloads' own seeds.
+def _edge_gen(wid: int, key: str) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(SEED_BASE + 1000 * wid + 500 + _K[key])
+    return g
+
+
+def make_saturating_inputs(shape: MLPShape, wid: int, z_std: float = 24.0) -> dict:
+    """The block's inputs with fc1's weights drawn at std z_std / sqrt(H), so that the
+    pre-activations Z (or G, U) have std ~ z_std: over a few hundred thousand entries
+    |Z| reaches ~4.5 z_std, deep into the saturated tails of GELU and SiLU (past the
+    point where exp(|x|) overflows fp32).  Everything else as make_inputs."""
+    d = make_inputs(shape, wid)
+    t, Fs, H = shape.tp, shape.fs, shape.hidden
+    w1_shape = (t, 2, Fs, H) if shape.act == "swiglu" else (t, Fs, H)
+    w = torch.randn(w1_shape, generator=_edge_gen(wid, "W1"), dtype=torch.float32)
+    d["W1"] = w.mul_(z_std / float(H) ** 0.5).to(torch.bfloat16)
+    return d
+
+
+def make_zero_block_inputs(shape: MLPShape, wid: int) -> dict:
+    """make_inputs with exact-zero blocks: X rows [64, 192) (crossing a 128-row tile
+    boundary) and X columns [0, 32); dY rows [100, 228) and dY columns [32, 96)."""
+    d = make_inputs(shape, wid)
+    T, H = shape.tokens, shape.hidden
+    X, dY = d["X"].clone(), d["dY"].clone()
+    X[64:min(192, T)] = 0
+    X[:, :min(32, H)] = 0
+    dY[100:min(228, T)] = 0
+    dY[:, 32:min(96, H)] = 0
+    d["X"], d["dY"] = X, dY
+    return d
+
+
+LN_EDGE_KINDS = ("normal", "constant", "offset", "outlier")
+
+
+def make_ln_edge_rows(T: int, H: int, wid: int) -> torch.Tensor:
+    """A bf16 [T, H] LayerNorm input whose row r is of kind LN_EDGE_KINDS[r % 4]:
+    normal N(0,1); constant (one N(0,1) value repeated: variance 0); offset (1e3 + N(0,1):
+    a common offset 1000x the spread); outlier (N(0,1) with the first element set to 50,
+    a 50-sigma value where a row's statistics start)."""
+    g = _edge_gen(wid, "X")
+    x = torch.randn((T, H), generator=g, dtype=torch.float32)
+    c = torch.randn((T,), generator=g, dtype=torch.float32)
+    kind = torch.arange(T) % 4
+    x[kind == 1] = c[kind == 1][:, None].expand(-1, H)
+    x[kind == 2] += 1000.0
+    x[kind == 3, 0] = 50.0
+    return x.to(torch.bfloat16)

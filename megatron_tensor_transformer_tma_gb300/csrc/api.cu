@@ -125,10 +125,9 @@ struct mlpb_handle {
   bool accumulate;  // MLPB_FLAG_ACCUMULATE_GRADS: parameter gradients add into their outputs
   bool recompute;   // MLPB_FLAG_RECOMPUTE_ACT: the backward rewrites A from the saved Z
   bool fp8;         // MLPB_FLAG_FP8: E4M3 GEMMs, per-tensor power-of-two scales
+  bool bf16_out;    // MLPB_FLAG_BF16_OUT: Y, dX (and the LN backward's dXn, dX) in bf16
+  bool emulate;     // MLPB_FLAG_EMULATE_COPIES: the SP gathers / scatters as device copies
   uint64_t wait_ns;
-  // bias-grad split plans
-  int db2_splits, db1_splits;
-  int64_t db2_rows, db1_rows;
   int ln_blocks_per_shard;
   // second stream of the backward: db2 at the fork, then (after dgrad) dW2, db1 and dW1
   // beside dX, filling the GEMMs' tails
@@ -178,6 +177,16 @@ struct LaunchTimer {
 };
 
 mlpb_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLPB_OK : MLPB_ECUDA; }
+
+// One emulated sequence-parallel gather or scatter: a device copy, timed like a kernel
+// and counted apart from the algorithmic bytes (read + write).
+mlpb_status sp_copy(mlpb_handle* h, void* dst, const void* src, size_t bytes, cudaStream_t s,
+                    const char* name) {
+  LaunchTimer lt(h, s, name, 0.0, 2.0 * bytes);
+  cudaError_t e = launch_copy16(dst, src, bytes, h->num_sms, s);
+  lt.done();
+  return from_cuda(e);
+}
 
 GemmParams base_params(const mlpb_handle* h) {
   GemmParams p{};
@@ -255,15 +264,15 @@ mlpb_status f8_cast(mlpb_handle* h, const void* x, int batches, int64_t R, int64
 
 size_t ws_dz_bytes(const mlpb_handle* h) { return align256(static_cast<size_t>(h->T * h->F1 * 2)); }
 
-// Workspace of the bf16 path: dZ [T][F1] bf16, the bias sums' partials, then the tail
-// split's partial tiles (used by fc2 in the forward and by dX in the backward, beside the
-// bias sums on the other stream).
+// Rows of db1 partial sums: one per 32-row group of dZ (a warp's rows in the dgrad epilogue).
+size_t ws_db1_parts(const mlpb_handle* h) { return static_cast<size_t>(h->T / 32); }
+
+// Workspace of the bf16 path: dZ [T][F1] bf16, the db1 partial sums that the dgrad
+// epilogue writes ([T/32][F] fp32, with a bias), then the tail split's partial tiles (used
+// by fc2 in the forward and by dX in the backward).
 size_t ws_split_offset(const mlpb_handle* h) {
   size_t b = ws_dz_bytes(h);
-  if (h->cfg.has_bias) {
-    b += align256(static_cast<size_t>(h->db2_splits) * h->H * 4);
-    b += align256(static_cast<size_t>(h->db1_splits) * h->F * 4);
-  }
+  if (h->cfg.has_bias) b += align256(ws_db1_parts(h) * h->F * 4);
   return b;
 }
 
@@ -339,13 +348,28 @@ F8Layout f8_layout(const mlpb_handle* h, void* workspace) {
   return L;
 }
 
-void plan_colsum(int64_t R, int64_t C, int num_sms, int* splits, int64_t* rows) {
-  const int64_t chunks = std::max<int64_t>(1, cdiv(C, 512));
-  int64_t s = cdiv(4 * num_sms, chunks);
-  s = std::max<int64_t>(1, std::min<int64_t>(s, std::max<int64_t>(1, R / 16)));
-  int64_t rp = std::max<int64_t>(1, cdiv(R, s));
-  *rows = rp;
-  *splits = static_cast<int>(std::max<int64_t>(1, cdiv(R, rp)));
+
+// Regions of the emulated sequence-parallel exchange (MLPB_FLAG_EMULATE_COPIES), after
+// everything else: the gathered input [T][H] bf16, the gathered upstream gradient [T][H]
+// bf16, and the full output before its scatter [T][H] (fp32, or bf16 with bf16 outputs).
+struct CopyLayout {
+  void *xfull, *dyfull, *outfull;
+};
+
+size_t ws_copy_bytes(const mlpb_handle* h) {
+  if (!h->emulate) return 0;
+  const size_t TH = static_cast<size_t>(h->T * h->H);
+  return 2 * align256(2 * TH) + align256(4 * TH);
+}
+
+CopyLayout copy_layout(const mlpb_handle* h, void* workspace) {
+  const size_t TH = static_cast<size_t>(h->T * h->H);
+  uint8_t* b = static_cast<uint8_t*>(workspace) + ws_base_bytes(h) + ws_f8_bytes(h);
+  return CopyLayout{b, b + align256(2 * TH), b + 2 * align256(2 * TH)};
+}
+
+size_t ws_total_bytes(const mlpb_handle* h) {
+  return ws_base_bytes(h) + ws_f8_bytes(h) + ws_copy_bytes(h);
 }
 
 }  // namespace
@@ -373,9 +397,11 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   if (c.has_bias != 0 && c.has_bias != 1) return MLPB_EINVAL;
   if (c.seq_parallel_ln != 0 && c.seq_parallel_ln != 1) return MLPB_EINVAL;
   if ((c.flags & ~(MLPB_FLAG_FAULT_INJECT | MLPB_FLAG_ACCUMULATE_GRADS |
-                   MLPB_FLAG_RECOMPUTE_ACT | MLPB_FLAG_FP8)) != 0)
+                   MLPB_FLAG_RECOMPUTE_ACT | MLPB_FLAG_FP8 | MLPB_FLAG_BF16_OUT |
+                   MLPB_FLAG_EMULATE_COPIES)) != 0)
     return MLPB_EINVAL;
   if (c.seq_parallel_ln && !(c.ln_eps > 0.f)) return MLPB_EINVAL;
+  if ((c.flags & MLPB_FLAG_EMULATE_COPIES) && !c.seq_parallel_ln) return MLPB_EUNSUPPORTED;
   if (c.tokens % 128 != 0 || c.hidden % 64 != 0) return MLPB_EUNSUPPORTED;
   if (c.ffn % c.tp != 0 || (c.ffn / c.tp) % 8 != 0) return MLPB_EUNSUPPORTED;
   if (c.act == MLPB_ACT_SWIGLU && c.has_bias) return MLPB_EUNSUPPORTED;
@@ -402,6 +428,8 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
   h->accumulate = (c.flags & MLPB_FLAG_ACCUMULATE_GRADS) != 0;
   h->recompute = (c.flags & MLPB_FLAG_RECOMPUTE_ACT) != 0;
   h->fp8 = (c.flags & MLPB_FLAG_FP8) != 0;
+  h->bf16_out = (c.flags & MLPB_FLAG_BF16_OUT) != 0;
+  h->emulate = (c.flags & MLPB_FLAG_EMULATE_COPIES) != 0;
   h->wait_ns = 1000000000ull;
   h->timing = false;
   h->d_err = nullptr;
@@ -442,8 +470,6 @@ mlpb_status mlpb_create(const mlpb_config* cfg, mlpb_handle** out) {
     mlpb_destroy(h);
     return MLPB_ECUDA;
   }
-  plan_colsum(h->T, h->H, h->num_sms, &h->db2_splits, &h->db2_rows);
-  plan_colsum(h->T, h->F, h->num_sms, &h->db1_splits, &h->db1_rows);
   // LN backward: two CTAs per SM, split evenly over the t sequence shards
   h->ln_blocks_per_shard =
       static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(2 * h->num_sms, h->t),
@@ -469,8 +495,7 @@ void mlpb_destroy(mlpb_handle* h) {
 
 mlpb_status mlpb_workspace_size(const mlpb_handle* h, size_t* bytes) {
   if (h == nullptr || bytes == nullptr) return MLPB_EINVAL;
-  *bytes = h->fp8 ? ws_base_bytes(h) + ws_f8_bytes(h)
-                  : std::max<size_t>(std::max(ws_backward_bytes(h), ws_ln_bytes(h)), 256);
+  *bytes = ws_total_bytes(h);
   return MLPB_OK;
 }
 
@@ -482,26 +507,27 @@ mlpb_status mlpb_saved_size(const mlpb_handle* h, size_t* z_bytes, size_t* a_byt
 }
 
 static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
-                                const void* W2, const void* b2, float* Y, void* Zsaved,
+                                const void* W2, const void* b2, void* Y, void* Zsaved,
                                 void* Asaved, const void* resid, void* workspace,
                                 cudaStream_t s);
 static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, const void* W2,
                                const void* Zsaved, const void* Asaved, const void* dY,
-                               float* dX, float* dW1, float* dW2, float* db1, float* db2,
+                               void* dX, float* dW1, float* dW2, float* db1, float* db2,
                                void* workspace, cudaStream_t s);
 static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
-                               const float* mean, const float* rstd, const float* dXn,
-                               const void* dres, float* dX, float* dgamma, float* dbeta,
+                               const float* mean, const float* rstd, const void* dXn,
+                               const void* dres, void* dX, float* dgamma, float* dbeta,
                                void* workspace, cudaStream_t s);
 
 mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const void* b1,
-                         const void* W2, const void* b2, float* Y, void* Zsaved, void* Asaved,
+                         const void* W2, const void* b2, void* Y, void* Zsaved, void* Asaved,
                          void* workspace, mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;
   const bool bias = h->cfg.has_bias != 0;
   if (!W1 || !W2) return MLPB_EINVAL;
   if (h->T > 0 && (!X || !Y || !Zsaved || !Asaved)) return MLPB_EINVAL;  // T = 0: empty tensors
-  if (h->T > 0 && h->fp8 && (!workspace || !aligned16(workspace))) return MLPB_EINVAL;
+  if (h->T > 0 && (h->fp8 || h->emulate) && (!workspace || !aligned16(workspace)))
+    return MLPB_EINVAL;
   if (bias != (b1 != nullptr) || bias != (b2 != nullptr)) return MLPB_EINVAL;
   for (const void* p : {X, W1, W2, static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
                         static_cast<const void*>(Asaved), b1, b2})
@@ -519,7 +545,7 @@ mlpb_status mlpb_forward(mlpb_handle* h, const void* X, const void* W1, const vo
 // second stream beside X's and fc1 measured no faster: a persistent GEMM CTA holds 225 KB
 // of shared memory, so the casts cannot share its SMs.)
 static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, const void* b1,
-                              const void* W2, const void* b2, float* Y, void* Zsaved,
+                              const void* W2, const void* b2, void* Y, void* Zsaved,
                               void* Asaved, const void* resid, void* workspace, cudaStream_t s) {
   const bool bias = h->cfg.has_bias != 0;
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
@@ -564,6 +590,7 @@ static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, con
   q.bias = static_cast<const __nv_bfloat16*>(b2);
   q.aux = static_cast<const __nv_bfloat16*>(resid);
   q.out0 = Y;
+  q.out_bf16 = h->bf16_out ? 1 : 0;
   q.amax_a = am + kAmaxA;
   q.amax_b = am + kAmaxW2;
 
@@ -591,12 +618,12 @@ static mlpb_status forward_f8(mlpb_handle* h, const void* X, const void* W1, con
   if (st != MLPB_OK) return st;
   // ---- fc2 (the sum over shards accumulates in one TMEM tile; one scale for all shards)
   return run_gemm_f8(h, GemmKind::FC2, ta2, tb2, q, s, "fc2_f8", 2.0 * T * H * F,
-                     1.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
-                         (resid ? 2.0 * T * H : 0.0));
+                     1.0 * (T * F + H * F) + (h->bf16_out ? 2.0 : 4.0) * T * H +
+                         (bias ? 2.0 * H : 0.0) + (resid ? 2.0 * T * H : 0.0));
 }
 
-static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
-                                const void* W2, const void* b2, float* Y, void* Zsaved,
+static mlpb_status forward_core(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                                const void* W2, const void* b2, void* Y, void* Zsaved,
                                 void* Asaved, const void* resid, void* workspace,
                                 cudaStream_t s) {
   if (h->fp8) return forward_f8(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, resid, workspace, s);
@@ -662,14 +689,40 @@ static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, c
   q.bias = static_cast<const __nv_bfloat16*>(b2);
   q.aux = static_cast<const __nv_bfloat16*>(resid);
   q.out0 = Y;
+  q.out_bf16 = h->bf16_out ? 1 : 0;
   plan_tail_split(h, q, ws_split_partial(h, workspace));
   return run_gemm(h, GemmKind::FC2, true, ta2, tb2, q, s, "fc2", 2.0 * T * H * F,
-                  2.0 * (T * F + H * F) + 4.0 * T * H + (bias ? 2.0 * H : 0.0) +
-                      (resid ? 2.0 * T * H : 0.0));
+                  2.0 * (T * F + H * F) + (h->bf16_out ? 2.0 : 4.0) * T * H +
+                      (bias ? 2.0 * H : 0.0) + (resid ? 2.0 * T * H : 0.0));
 }
 
+// The forward of validated arguments.  With emulated sequence-parallel copies, the input's
+// sequence shards are first gathered into one [T][H] tensor (the all-gather in front of
+// fc1), and fc2's output -- already summed over the tensor-parallel shards in the
+// accumulator -- is scattered back to the rows' own shards (the reduce-scatter's scatter).
+static mlpb_status forward_impl(mlpb_handle* h, const void* X, const void* W1, const void* b1,
+                                const void* W2, const void* b2, void* Y, void* Zsaved,
+                                void* Asaved, const void* resid, void* workspace,
+                                cudaStream_t s) {
+  if (!h->emulate)
+    return forward_core(h, X, W1, b1, W2, b2, Y, Zsaved, Asaved, resid, workspace, s);
+  const CopyLayout C = copy_layout(h, workspace);
+  const size_t TH = static_cast<size_t>(h->T * h->H);
+  mlpb_status st = sp_copy(h, C.xfull, X, 2 * TH, s, "sp_gather_x");
+  if (st == MLPB_OK)
+    st = forward_core(h, C.xfull, W1, b1, W2, b2, C.outfull, Zsaved, Asaved, resid, workspace,
+                      s);
+  if (st == MLPB_OK) st = sp_copy(h, Y, C.outfull, (h->bf16_out ? 2 : 4) * TH, s, "sp_scatter_y");
+  return st;
+}
+
+static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, const void* W2,
+                                 const void* Zsaved, void* Asaved, const void* dY, void* dX,
+                                 float* dW1, float* dW2, float* db1, float* db2, void* workspace,
+                                 cudaStream_t s);
+
 mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const void* W2,
-                          const void* Zsaved, void* Asaved, const void* dY, float* dX,
+                          const void* Zsaved, void* Asaved, const void* dY, void* dX,
                           float* dW1, float* dW2, float* db1, float* db2, void* workspace,
                           mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;
@@ -698,13 +751,36 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     return st;
   }
 
+  if (!h->emulate)
+    return backward_core(h, X, W1, W2, Zsaved, Asaved, dY, dX, dW1, dW2, db1, db2, workspace, s);
+  // emulated sequence parallelism: gather the input again (for dW1) and the upstream
+  // gradient (the all-gather that is the reduce-scatter's backward), scatter dX's rows
+  const CopyLayout C = copy_layout(h, workspace);
+  const size_t TH = static_cast<size_t>(T * H);
+  st = sp_copy(h, C.xfull, X, 2 * TH, s, "sp_gather_x");
+  if (st == MLPB_OK) st = sp_copy(h, C.dyfull, dY, 2 * TH, s, "sp_gather_dy");
+  if (st == MLPB_OK)
+    st = backward_core(h, C.xfull, W1, W2, Zsaved, Asaved, C.dyfull, C.outfull, dW1, dW2, db1,
+                       db2, workspace, s);
+  if (st == MLPB_OK)
+    st = sp_copy(h, dX, C.outfull, (h->bf16_out ? 2 : 4) * TH, s, "sp_scatter_dx");
+  return st;
+}
+
+// The backward of validated arguments with T > 0.
+static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, const void* W2,
+                                 const void* Zsaved, void* Asaved, const void* dY, void* dX,
+                                 float* dW1, float* dW2, float* db1, float* db2, void* workspace,
+                                 cudaStream_t s) {
   if (h->fp8)
     return backward_f8(h, X, W1, W2, Zsaved, Asaved, dY, dX, dW1, dW2, db1, db2, workspace, s);
+  const bool bias = h->cfg.has_bias != 0;
+  const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
+  const int acc = h->accumulate ? 1 : 0;
+  mlpb_status st = MLPB_OK;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* dZ = ws;
-  float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
-  float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
-                                          align256(static_cast<size_t>(h->db2_splits) * H * 4));
+  float* part1 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));  // db1 partials [T/32][F]
   const bool recompute = h->recompute;
 
   // Tensor maps of all four GEMMs first: an encoding error launches nothing.
@@ -732,9 +808,8 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 
   // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
-    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H, 2);
-    cudaError_t e =
-        launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s2, acc);
+    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
+    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -750,9 +825,11 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
     p.out0 = dZ;
     p.out1 = recompute ? Asaved : nullptr;
+    p.colsum = bias ? part1 : nullptr;
     st = run_gemm(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, false, tdgA,
                   tdgB, p, s, h->swiglu ? "dgrad_swiglu" : "dgrad_gelu", 2.0 * T * F * H,
-                  2.0 * (T * H + F * H + 2 * T * F1) + (recompute ? 2.0 * T * F : 0.0));
+                  2.0 * (T * H + F * H + 2 * T * F1) + (recompute ? 2.0 * T * F : 0.0) +
+                      (bias ? 4.0 * ws_db1_parts(h) * F : 0.0));
   }
   if (st == MLPB_OK && (cudaEventRecord(h->ev_dz, s) != cudaSuccess ||
                         cudaStreamWaitEvent(s2, h->ev_dz, 0) != cudaSuccess))
@@ -773,11 +850,11 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
                   2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
 
-  // ---- [s2] db1 = sum_t dZ
+  // ---- [s2] db1 = sum_t dZ: the dgrad epilogue's per-warp column sums, added in row order
   if (st == MLPB_OK && bias) {
-    LaunchTimer lt(h, s2, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
-    cudaError_t e =
-        launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s2, acc);
+    const int np = static_cast<int>(ws_db1_parts(h));
+    LaunchTimer lt(h, s2, "db1_sum", 0.0, 4.0 * np * F + 4.0 * (1 + acc) * F);
+    cudaError_t e = launch_sum_partials(part1, np, F, db1, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -804,9 +881,10 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
+    p.out_bf16 = h->bf16_out ? 1 : 0;
     plan_tail_split(h, p, ws_split_partial(h, workspace));
     st = run_gemm(h, GemmKind::DX, false, tdxA, tdxB, p, s, "dgrad_x", 2.0 * T * H * F1,
-                  2.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+                  2.0 * (T * F1 + F1 * H) + (h->bf16_out ? 2.0 : 4.0) * T * H);
   }
 
   // Join: the caller's stream waits for s2 whatever happened above.
@@ -825,16 +903,14 @@ mlpb_status mlpb_backward(mlpb_handle* h, const void* X, const void* W1, const v
 // casts cannot share its SMs.)
 static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, const void* W2,
                                const void* Zsaved, const void* Asaved, const void* dY,
-                               float* dX, float* dW1, float* dW2, float* db1, float* db2,
+                               void* dX, float* dW1, float* dW2, float* db1, float* db2,
                                void* workspace, cudaStream_t s) {
   const bool bias = h->cfg.has_bias != 0;
   const int64_t T = h->T, H = h->H, F = h->F, Fs = h->Fs, t = h->t, F1 = h->F1;
   const int acc = h->accumulate ? 1 : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* dZ = ws;
-  float* part2 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));
-  float* part1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part2) +
-                                          align256(static_cast<size_t>(h->db2_splits) * H * 4));
+  float* part1 = reinterpret_cast<float*>(ws + ws_dz_bytes(h));  // db1 partials [T/32][F]
   const F8Layout L = f8_layout(h, workspace);
   uint32_t* am = L.amax;
 
@@ -872,13 +948,15 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.amax_a = am + kAmaxDY;
     p.amax_b = am + kAmaxW2;
     p.amax_out = am + kAmaxDZ;
+    p.colsum = bias ? part1 : nullptr;
     st = run_gemm_f8(h, h->swiglu ? GemmKind::DGRAD_SWIGLU : GemmKind::DGRAD_GELU, tdA, tdB,
                      p, s, h->swiglu ? "dgrad_swiglu_f8" : "dgrad_gelu_f8", 2.0 * T * F * H,
-                     1.0 * (T * H + F * H) + 4.0 * T * F1);
+                     1.0 * (T * H + F * H) + 4.0 * T * F1 +
+                         (bias ? 4.0 * ws_db1_parts(h) * F : 0.0));
   }
   if (st == MLPB_OK && bias) {  // db2 = sum_t dY on the bf16 dY
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H, 2);
-    cudaError_t e = launch_colsum_bf16(dY, T, H, h->db2_splits, h->db2_rows, part2, db2, s, acc);
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
+    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, s, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -894,10 +972,11 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     p.num_n_tiles = static_cast<int>(cdiv(H, kBN));
     p.num_kb = static_cast<int>(cdiv(F1, kBK8));
     p.out0 = dX;
+    p.out_bf16 = h->bf16_out ? 1 : 0;
     p.amax_a = am + kAmaxDZ;
     p.amax_b = am + kAmaxW1;
     st = run_gemm_f8(h, GemmKind::DX, txA, txB, p, s, "dgrad_x_f8", 2.0 * T * H * F1,
-                     1.0 * (T * F1 + F1 * H) + 4.0 * T * H);
+                     1.0 * (T * F1 + F1 * H) + (h->bf16_out ? 2.0 : 4.0) * T * H);
   }
   // ---- dW2_i = dY^T A_i  (M = H, N = F by shard, K = T)
   if (st == MLPB_OK)
@@ -916,9 +995,10 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     st = run_gemm_f8(h, GemmKind::WGRAD_W2, tw2A, tw2B, p, s, "wgrad_w2_f8", 2.0 * H * F * T,
                      1.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
-  if (st == MLPB_OK && bias) {  // db1 = sum_t dZ on the bf16 dZ
-    LaunchTimer lt(h, s, "colsum_db1", 0.0, 2.0 * T * F + 4.0 * (1 + acc) * F, 2);
-    cudaError_t e = launch_colsum_bf16(dZ, T, F, h->db1_splits, h->db1_rows, part1, db1, s, acc);
+  if (st == MLPB_OK && bias) {  // db1 = sum_t dZ: the dgrad epilogue's per-warp column sums
+    const int np = static_cast<int>(ws_db1_parts(h));
+    LaunchTimer lt(h, s, "db1_sum", 0.0, 4.0 * np * F + 4.0 * (1 + acc) * F);
+    cudaError_t e = launch_sum_partials(part1, np, F, db1, s, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -959,8 +1039,8 @@ mlpb_status mlpb_layernorm_sp_fwd(mlpb_handle* h, const void* X, const void* gam
 }
 
 mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gamma,
-                                  const float* mean, const float* rstd, const float* dXn,
-                                  float* dX, float* dgamma, float* dbeta, void* workspace,
+                                  const float* mean, const float* rstd, const void* dXn,
+                                  void* dX, float* dgamma, float* dbeta, void* workspace,
                                   mlpb_stream_t stream) {
   if (h == nullptr || !gamma || !dgamma || !dbeta) return MLPB_EINVAL;
   if (h->T > 0 && (!X || !mean || !rstd || !dXn || !dX || !workspace))
@@ -975,8 +1055,8 @@ mlpb_status mlpb_layernorm_sp_bwd(mlpb_handle* h, const void* X, const void* gam
 
 // LayerNorm backward of validated arguments; `dres` (bf16 [T][H] or NULL) is added to dX.
 static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
-                               const float* mean, const float* rstd, const float* dXn,
-                               const void* dres, float* dX, float* dgamma, float* dbeta,
+                               const float* mean, const float* rstd, const void* dXn,
+                               const void* dres, void* dX, float* dgamma, float* dbeta,
                                void* workspace, cudaStream_t s) {
   const int64_t T = h->T, H = h->H;
   const int nblk = h->t * h->ln_blocks_per_shard;
@@ -990,10 +1070,11 @@ static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
     if (e == cudaSuccess) e = launch_fill_zero(dbeta, static_cast<size_t>(H * 4), s);
     return from_cuda(e);
   }
+  const double gb = h->bf16_out ? 2.0 : 4.0;  // bytes of a dXn / dX element
   LaunchTimer lt(h, s, "ln_bwd", 0.0,
-                 (dres ? 12.0 : 10.0) * T * H + 8.0 * T + 10.0 * H);
-  cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dres, dX, pg, pb, T, H, h->t,
-                                h->ln_blocks_per_shard, h->d_err, h->wait_ns, s);
+                 (2.0 + 2.0 * gb + (dres ? 2.0 : 0.0)) * T * H + 8.0 * T + 10.0 * H);
+  cudaError_t e = launch_ln_bwd(X, gamma, mean, rstd, dXn, dres, dX, h->bf16_out, pg, pb, T, H,
+                                h->t, h->ln_blocks_per_shard, h->d_err, h->wait_ns, s);
   lt.done();
   if (e == cudaSuccess) {
     LaunchTimer lt2(h, s, "ln_bwd_param_reduce", 0.0, 8.0 * nblk * H + 8.0 * (1 + acc) * H, 1);
@@ -1005,7 +1086,7 @@ static mlpb_status ln_bwd_impl(mlpb_handle* h, const void* X, const void* gamma,
 
 mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma,
                                 const void* beta, const void* W1, const void* b1,
-                                const void* W2, const void* b2, float* Y, void* Xn, float* mean,
+                                const void* W2, const void* b2, void* Y, void* Xn, float* mean,
                                 float* rstd, void* Zsaved, void* Asaved, void* workspace,
                                 mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;
@@ -1018,7 +1099,8 @@ mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma
                         static_cast<const void*>(Y), static_cast<const void*>(Zsaved),
                         static_cast<const void*>(Asaved), b1, b2})
     if (p && !aligned16(p)) return MLPB_EINVAL;
-  if (h->T > 0 && h->fp8 && (!workspace || !aligned16(workspace))) return MLPB_EINVAL;
+  if (h->T > 0 && (h->fp8 || h->emulate) && (!workspace || !aligned16(workspace)))
+    return MLPB_EINVAL;
   if (h->T == 0) return MLPB_OK;
   mlpb_status st = mlpb_layernorm_sp_fwd(h, X, gamma, beta, Xn, mean, rstd, stream);
   if (st != MLPB_OK) return st;
@@ -1029,7 +1111,7 @@ mlpb_status mlpb_branch_forward(mlpb_handle* h, const void* X, const void* gamma
 mlpb_status mlpb_branch_backward(mlpb_handle* h, const void* X, const void* gamma,
                                  const void* W1, const void* W2, const void* Xn,
                                  const float* mean, const float* rstd, const void* Zsaved,
-                                 void* Asaved, const void* dY, float* dX, float* dW1,
+                                 void* Asaved, const void* dY, void* dX, float* dW1,
                                  float* dW2, float* db1, float* db2, float* dgamma, float* dbeta,
                                  void* workspace, mlpb_stream_t stream) {
   if (h == nullptr) return MLPB_EINVAL;

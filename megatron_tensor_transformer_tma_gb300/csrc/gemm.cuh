@@ -164,6 +164,25 @@ __device__ __forceinline__ void add_f32x32(const float* p, int nvalid, float (&v
   }
 }
 
+// Column sums over a warp's 32 rows: on entry lane l holds v[0..32) of its own row, on
+// exit it returns the sum over the 32 lanes of column l.  Each of five exchange rounds
+// halves the columns a lane keeps (16 + 8 + 4 + 2 + 1 shuffles); the order of the adds is
+// fixed, so the sums are reproducible.  v is overwritten.
+__device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = upper ? v[j] : v[j + w];
+      const float keep = upper ? v[j + w] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ void tmem_load_f32x32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
@@ -189,12 +208,15 @@ __device__ __forceinline__ void track_amax(const float (&v)[32], int nv, float& 
     if (e < nv) am = fmaxf(am, fabsf(v[e]));
 }
 
-// Epilogue of one 128 x 256 tile for the calling thread's row.  `tacc` is the TMEM
-// address of the accumulator at this warp's lane quarter.  All branches that skip
-// tcgen05.ld are uniform across the warp.
+// Epilogue of one 128 x 256 tile for the calling thread's row, over the 32-column chunks
+// [c0, c1) of the tile (group g of kEpiGroups takes chunks [8g, 8g + 8) / kEpiGroups; the
+// SwiGLU tile's 4 gate/up chunk pairs are split the same way).  `tacc` is the TMEM address
+// of the accumulator at this warp's lane quarter.  All branches that skip tcgen05.ld are
+// uniform across the warp.
 template <GemmKind K, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, int nt,
-                                              const GemmParams& p, float sc, float& am) {
+                                              const GemmParams& p, float sc, float& am, int grp) {
+  const int c0 = grp * (kBN / 32) / kEpiGroups, c1 = (grp + 1) * (kBN / 32) / kEpiGroups;
   const int m = mt * kBM + row;
   const bool row_ok = m < p.M;
   if constexpr (K == GemmKind::FC1_GELU) {
@@ -202,7 +224,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * p.F;
     __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.F) break;
       float v[32];
@@ -230,7 +252,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F +
                        static_cast<size_t>(i) * p.Fs;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = c0 / 2; c < c1 / 2; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float g[32], u[32];
@@ -250,9 +272,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     }
   } else if constexpr (K == GemmKind::FC2 || K == GemmKind::DX) {
     const int n0 = nt * kBN;
-    float* Y = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H;
+    const size_t yo = static_cast<size_t>(m) * p.H;  // row m of Y (fp32, or bf16 with out_bf16)
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -270,7 +292,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] += r[e];
       }
-      if (row_ok) store_f32x32(Y + col, nv, v);
+      if (row_ok) {
+        if (p.out_bf16)
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + yo + col, nv, v);
+        else
+          store_f32x32(static_cast<float*>(p.out0) + yo + col, nv, v);
+      }
     }
   } else if constexpr (K == GemmKind::DGRAD_GELU) {
     const int i = nt / p.tiles_per_shard;
@@ -281,7 +308,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     // recomputation: A = gelu(Z) from the saved Z, for the dW2 GEMM that follows
     __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + base : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32], z[32];
@@ -300,6 +327,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         store_bf16x32(dZ + jc, nv, v);
         if constexpr (F8) track_amax(v, nv, am);
       }
+      if (p.colsum != nullptr) {  // db1 partials: column sums of the stored (bf16) dZ
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          v[e] = row_ok ? __bfloat162float(__float2bfloat16_rn(v[e])) : 0.0f;
+        const float cs = warp_column_sums(v);
+        const int lane = threadIdx.x & 31;
+        if (lane < nv)
+          p.colsum[static_cast<size_t>(m >> 5) * p.F + static_cast<size_t>(i) * p.Fs + jc + lane] = cs;
+      }
     }
   } else if constexpr (K == GemmKind::DGRAD_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
@@ -312,7 +348,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
                                     static_cast<size_t>(i) * p.Fs
                               : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float da[32];
@@ -348,7 +384,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
     float* dW = static_cast<float*>(p.out0) + (static_cast<size_t>(i) * p.H + m) * p.Fs;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32];
@@ -367,7 +403,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int j = m - i * p.Fs;
     float* dW = static_cast<float*>(p.out0) + static_cast<size_t>(i) * p.H * p.Fs + j;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -389,7 +425,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int n0 = nt * kBN;
     float* dW = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c0; c < c1; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -514,7 +550,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 8);  // four epilogue warps in each CTA
+      mbar_init(tempty0 + 8 * b, 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -548,14 +584,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool skip_once = p.fault_inject != 0 && cid == 0 && leader;
-      for (int u = cid; u < num_units; u += nclusters) {
+      int it = 0;
+      for (int u = cid; u < num_units; u += nclusters, ++it) {
         int st, kb0, kb1, part;
         unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
         int mp, nt;
         tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * 2 + rank;
+        // whole tiles of odd iterations walk K backwards (kReverseK): the pair's next tile
+        // shares an operand panel with this one and starts on the k-blocks just read
+        const bool rev = kReverseK && part < 0 && (it & 1) != 0;
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int i = kb0; i < kb1; ++i) {
+          const int kb = rev ? kb0 + kb1 - 1 - i : i;
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -604,7 +645,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {  // stage order; the producer chose the k-blocks
           if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull) ||
               !wait_bounded(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
             ok = false;
@@ -662,6 +703,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;  // column group: warps 2-5 group 0, warps 6-9 group 1
     const int row = quarter * 32 + lane;
     float sc = 1.0f;  // FP8: 2^-(k_a + k_b), exact
     if constexpr (F8) sc = ldexpf(1.0f, -(e4m3_scale_exp(*p.amax_a) + e4m3_scale_exp(*p.amax_b)));
@@ -687,13 +729,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    ((static_cast<size_t>(st - split_start) * split + part) * 2 + rank) * (kBM * kBN) +
                    static_cast<size_t>(row) * kBN;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = grp * (kBN / 32) / kEpiGroups; c < (grp + 1) * (kBN / 32) / kEpiGroups;
+             ++c) {
           float v[32];
           load_acc<F8>(tacc + c * 32, v, sc);
           store_f32x32(P + c * 32, 32, v);
         }
       } else {
-        epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am);
+        epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am, grp);
       }
       if constexpr (F8) {
         if (p.amax_out != nullptr) {  // non-negative floats order like their bit patterns

@@ -53,8 +53,9 @@ cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
 
 // Sums the tail tiles' partial K-ranges in part order and applies the fp32 epilogue of
 // FC2 / DX / WGRAD_W1: Y[m][n] = ((sum_p P_p) + bias[n]) + resid[m][n] (bias, resid
-// optional), or Y[m][n] += sum_p P_p when accumulating.  Y is [M][H] (dW1: M = F1).  A CTA
-// covers 8 rows x 256 columns of one CTA half of one tile; a thread 8 columns.
+// optional), or Y[m][n] += sum_p P_p when accumulating.  Y is [M][H] (dW1: M = F1), fp32,
+// or bf16 for FC2 / DX with out_bf16.  A CTA covers 8 rows x 256 columns of one CTA half
+// of one tile; a thread 8 columns.
 __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
   const int tiles_rows = kBM / 8;  // row groups a CTA half
   const int j = blockIdx.x / (2 * tiles_rows);
@@ -96,6 +97,12 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
       v[2 * e] += f.x;
       v[2 * e + 1] += f.y;
     }
+  }
+  if (p.out_bf16) {  // one rounding of the finished fp32 sum
+    __nv_bfloat16* Yb = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * p.H + n;
+    st_global_v4(Yb, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7])));
+    return;
   }
   float* Y = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H + n;
   if (p.accumulate) {

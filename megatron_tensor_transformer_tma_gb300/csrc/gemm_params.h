@@ -23,7 +23,20 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;  // k-block depth: 64 bf16 = 128-byte K-major rows (128-byte swizzle;
                          // 32-deep blocks with a 64-byte swizzle measured much slower)
 constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x kBK(K) MN-major box, 8 KB
-constexpr int kGemmThreads = 192;
+// Epilogue warps per CTA: 4 (one per TMEM lane quarter, each drains all 256 columns of
+// its 32 rows) or 8 (two per lane quarter, each drains 128 of the columns).
+#ifndef MLPB_EPI_WARPS
+#define MLPB_EPI_WARPS 4
+#endif
+constexpr int kEpiWarps = MLPB_EPI_WARPS;
+static_assert(kEpiWarps == 4 || kEpiWarps == 8, "4 or 8 epilogue warps");
+constexpr int kEpiGroups = kEpiWarps / 4;       // column groups of a tile
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA / relay, epilogue
+// Whole tiles of a pair's odd iterations walk their K range backwards (1) or not (0).
+#ifndef MLPB_REVERSE_K
+#define MLPB_REVERSE_K 0
+#endif
+constexpr bool kReverseK = MLPB_REVERSE_K != 0;
 constexpr int kTmemCols = 512;
 constexpr int kClusterM = 2;  // CTAs per cluster: the pair along M
 
@@ -49,6 +62,7 @@ struct GemmParams {
   uint64_t wait_ns;
   int fault_inject;
   int accumulate;  // weight-gradient kinds: add into the fp32 output instead of overwriting
+  int out_bf16;    // FC2, DX: write Y / dX as bf16 (rounded once, from the fp32 sum)
   // FP8 (E4M3) variants: the amax words of the two operands (their power-of-two scales
   // are derived from them), and where FC1 / DGRAD record the amax of the bf16 A / dZ
   // they write (the next GEMMs' operand)
@@ -62,6 +76,9 @@ struct GemmParams {
   int split;
   int split_start;
   float* partial;
+  // DGRAD_GELU with a bias: each warp writes the column sums of its 32 rows of the bf16 dZ
+  // it stores, colsum[m / 32][f] ([T/32][F] fp32), for the db1 reduction; NULL: none.
+  float* colsum;
 };
 
 // FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.

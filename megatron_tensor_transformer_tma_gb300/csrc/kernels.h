@@ -35,10 +35,16 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int accumulate = 0);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s, int accumulate = 0);
+// reduce.cu: the same column sums in one launch (clusters of 8 CTAs reduce through
+// distributed shared memory); C % 8 == 0, no scratch.
+cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out,
+                                  cudaStream_t s, int accumulate = 0);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
                                  float* out_a, float* out_b, cudaStream_t s, int accumulate = 0);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
+// reduce.cu: a device copy of `bytes` (a multiple of 16, both pointers 16-byte aligned).
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s);
 
 // layernorm.cu: rows streamed through a shared-memory ring by TMA bulk copies; bounded
 // waits report to `err`.
@@ -46,11 +52,12 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
                           float* mean, float* rstd, int64_t T, int64_t H, float eps, int num_sms,
                           uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 // dres (bf16 [T][H], or NULL) is added to dX: the gradient of a residual around the
-// normalised branch.  dXn may equal dX (in place, row by row).
+// normalised branch.  dXn and dX are fp32, or bf16 with bf16_grads.  dXn may equal dX
+// (in place, row by row).
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
-                          const float* dXn, const void* dres, float* dX, float* part_dg,
-                          float* part_db, int64_t T, int64_t H, int shards, int blocks_per_shard,
-                          uint32_t* err, uint64_t wait_ns, cudaStream_t s);
+                          const void* dXn, const void* dres, void* dX, bool bf16_grads,
+                          float* part_dg, float* part_db, int64_t T, int64_t H, int shards,
+                          int blocks_per_shard, uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 
 // fp8.cu: *amax = max(*amax, max|in|) over n bf16 values (n % 8 == 0), as fp32 bits.
 cudaError_t launch_amax_bf16(const void* in, int64_t n, uint32_t* amax, int num_sms,

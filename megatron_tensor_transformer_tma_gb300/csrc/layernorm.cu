@@ -6,9 +6,9 @@
 // of the row (kVpt vectors), so every global store is coalesced.  256-thread CTAs, two
 // or more per SM, so that several rows' reduction chains overlap on every SM.
 //
-// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row one block
-// reduction of shifted sums gives the mean and the biased variance of the
-// register-resident row; Xn = (x - mu) rstd gamma + beta in bf16.
+// Forward: persistent grid, CTA c handles rows c, c + grid, ...; per row two block
+// reductions (the sum, then the squared deviations from the mean) give the mean and the
+// biased variance of the register-resident row; Xn = (x - mu) rstd gamma + beta in bf16.
 // Sequence shard s owns rows [s T/t, (s+1) T/t); rows are independent, so the forward
 // needs no shard structure and the emulated all-gather is the row layout of Xn itself.
 //
@@ -78,11 +78,12 @@ __device__ __forceinline__ void st_f32x8(float* p, const float* o) {
 }
 
 // ------------------------------------------------------------------ forward
-// Statistics from one pass of shifted sums: with K = the row's first element,
-// S1 = sum (x - K) and S2 = sum (x - K)^2 give mean = K + S1/H and the biased variance
-// S2/H - (S1/H)^2.  Shifting by a value of the row keeps the subtraction well conditioned
-// (the textbook "shifted data" variance), and it needs a single block reduction and about
-// six instructions per element, which is what keeps this kernel memory-bound.
+// Row statistics by the textbook two-pass method over the register-resident row: one
+// block reduction of the sum gives the mean, a second of the squared deviations from
+// that mean gives the biased variance.  Unlike a single pass of (shifted) sums of
+// squares, nothing large is subtracted, so a row with a common offset far larger than
+// its spread, or with one far outlier, keeps its variance to fp32 rounding; per element
+// it costs an add, a subtract and an FMA, and per row one more block reduction.
 template <int kVpt>
 __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
@@ -90,14 +91,14 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     float* __restrict__ mean, float* __restrict__ rstd, int64_t T, int H, float eps, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnFwdThreads;
-  __shared__ float sh[2 * NT / 32];
+  __shared__ float sh[NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
   const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int64_t n_mine = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
   const WaitCtx wc{&abort_flag, err, wait_ns};
-  const float inv_h = 1.0f / static_cast<float>(H);
+  const float hf = static_cast<float>(H);
 
   if (threadIdx.x == 0) {
     abort_flag = 0u;
@@ -130,9 +131,8 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
     int ok = wait_bounded(bar0 + 8 * b, par, wc, kSiteLnFull) ? 1 : 0;
     if (!__syncthreads_and(ok)) break;
     const int64_t row = blockIdx.x + i * gridDim.x;
-    const float K = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ln_smem + b * row_bytes));
     float v[kVpt][8];
-    float s[2] = {0.f, 0.f};
+    float sum[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int vi = threadIdx.x + k * NT;
@@ -140,16 +140,10 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       uint4 u = make_uint4(0, 0, 0, 0);
       if (in) u = ld_shared_v4(b * row_bytes + vi * 16);
       bf16x8_to_f32(u, v[k]);
-      if (in) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = v[k][e] - K;
-          s[0] += d;
-          s[1] = fmaf(d, d, s[1]);
-        }
-      }
+      for (int e = 0; e < 8; ++e) sum[0] += v[k][e];  // zero beyond the row
     }
-    block_sum<NT, 2>(s, sh);  // every thread has read buffer b once this returns
+    block_sum<NT, 1>(sum, sh);  // every thread has read buffer b once this returns
     if (threadIdx.x == 0 && issued < n_mine) {
       const int64_t nrow = blockIdx.x + issued * gridDim.x;
       fence_proxy_async_smem();
@@ -157,18 +151,27 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
       bulk_load(buf0 + b * row_bytes, X + nrow * H, row_bytes, bar0 + 8 * b);
     }
     ++issued;
-    const float m1 = s[0] * inv_h;
-    const float var = fmaxf(fmaf(-m1, m1, s[1] * inv_h), 0.f);
-    const float mu = K + m1;
+    const float mu = sum[0] / hf;
+    float ssd[1] = {0.f};  // second pass: squared deviations from the row mean
+#pragma unroll
+    for (int k = 0; k < kVpt; ++k) {
+      if ((threadIdx.x + k * NT) * 8 >= H) continue;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = v[k][e] - mu;
+        ssd[0] = fmaf(d, d, ssd[0]);
+      }
+    }
+    block_sum<NT, 1>(ssd, sh);
+    const float var = ssd[0] / hf;
     const float r = rsqrtf(var + eps);
-    const float c0 = -mu * r;
 #pragma unroll
     for (int k = 0; k < kVpt; ++k) {
       const int c = (threadIdx.x + k * NT) * 8;
       if (c >= H) continue;
       float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = fmaf(fmaf(v[k][e], r, c0), gm[k][e], bt[k][e]);
+      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[k][e] - mu) * r, gm[k][e], bt[k][e]);
       st_global_v4(Xn + row * H + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
     }
@@ -187,21 +190,24 @@ __global__ void __launch_bounds__(kLnFwdThreads) ln_fwd_kernel(
 
 // ------------------------------------------------------------------ backward
 // With kRes, dX also receives the residual branch's gradient dres (bf16 [T][H]):
-// dX = dres + LN'(dXn).  dXn and dX may be the same buffer: each row of dXn is copied
-// whole into shared memory (and waited for) before any element of that row of dX is
-// written, and no other CTA touches the row.
-template <int kVpt, bool kRes>
+// dX = dres + LN'(dXn).  With kBf16, dXn is read and dX written as bf16 (the block's
+// bf16-output mode; the arithmetic is the same fp32, with one rounding of dX at the end).
+// dXn and dX may be the same buffer: each row of dXn is copied whole into shared memory
+// (and waited for) before any element of that row of dX is written, and no other CTA
+// touches the row.
+template <int kVpt, bool kRes, bool kBf16>
 __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ gamma,
-    const float* __restrict__ mean, const float* __restrict__ rstd, const float* dXn,
-    const __nv_bfloat16* __restrict__ dres, float* dX, float* __restrict__ part_dg,
+    const float* __restrict__ mean, const float* __restrict__ rstd, const void* dXn,
+    const __nv_bfloat16* __restrict__ dres, void* dX, float* __restrict__ part_dg,
     float* __restrict__ part_db, int64_t rows_per_shard, int blocks_per_shard, int H, int nbuf,
     uint32_t* err, uint64_t wait_ns) {
   constexpr int NT = kLnBwdThreads;
+  constexpr uint32_t kGradBytes = kBf16 ? 2u : 4u;  // bytes of a dXn / dX element
   __shared__ float sh[2 * NT / 32];
   __shared__ uint32_t abort_flag;
   const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
-  const uint32_t row_bytes = static_cast<uint32_t>(H) * 6u;  // X bf16 then dXn fp32
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * (2u + kGradBytes);  // X, then dXn
   const uint32_t buf0 = smem_u32(ln_smem);
   const uint32_t bar0 = buf0 + nbuf * row_bytes;
   const int shard = blockIdx.x / blocks_per_shard;
@@ -215,7 +221,9 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
     const int64_t row = rbeg + bidx + i * blocks_per_shard;
     mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
     bulk_load(buf0 + b * row_bytes, X + row * H, xbytes, bar0 + 8 * b);
-    bulk_load(buf0 + b * row_bytes + xbytes, dXn + row * H, 4u * H, bar0 + 8 * b);
+    bulk_load(buf0 + b * row_bytes + xbytes,
+              static_cast<const uint8_t*>(dXn) + static_cast<size_t>(row) * H * kGradBytes,
+              kGradBytes * H, bar0 + 8 * b);
     // the residual gradient's row is read with plain loads in pass 2; start it towards L2
     if constexpr (kRes) bulk_prefetch_l2(dres + row * H, xbytes);
   };
@@ -241,12 +249,16 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
   // x and dy of vector vi of the row in buffer (xb, db)
   auto load_vec = [&](uint32_t xb, uint32_t db, int vi, float* x, float* dy) {
     bf16x8_to_f32(ld_shared_v4(xb + vi * 16), x);
-    const uint4 d0 = ld_shared_v4(db + vi * 32);
-    const uint4 d1 = ld_shared_v4(db + vi * 32 + 16);
-    dy[0] = __uint_as_float(d0.x); dy[1] = __uint_as_float(d0.y);
-    dy[2] = __uint_as_float(d0.z); dy[3] = __uint_as_float(d0.w);
-    dy[4] = __uint_as_float(d1.x); dy[5] = __uint_as_float(d1.y);
-    dy[6] = __uint_as_float(d1.z); dy[7] = __uint_as_float(d1.w);
+    if constexpr (kBf16) {
+      bf16x8_to_f32(ld_shared_v4(db + vi * 16), dy);
+    } else {
+      const uint4 d0 = ld_shared_v4(db + vi * 32);
+      const uint4 d1 = ld_shared_v4(db + vi * 32 + 16);
+      dy[0] = __uint_as_float(d0.x); dy[1] = __uint_as_float(d0.y);
+      dy[2] = __uint_as_float(d0.z); dy[3] = __uint_as_float(d0.w);
+      dy[4] = __uint_as_float(d1.x); dy[5] = __uint_as_float(d1.y);
+      dy[6] = __uint_as_float(d1.z); dy[7] = __uint_as_float(d1.w);
+    }
   };
 
   int64_t issued = nbuf < n_mine ? nbuf : n_mine;
@@ -309,7 +321,12 @@ __global__ void __launch_bounds__(kLnBwdThreads, 2) ln_bwd_kernel(
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(o[e], r[e]);  // a plain add, never an FMA
       }
-      st_f32x8(dX + row * H + vi * 8, o);
+      if constexpr (kBf16)
+        st_global_v4(static_cast<__nv_bfloat16*>(dX) + row * H + vi * 8,
+                     make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
+      else
+        st_f32x8(static_cast<float*>(dX) + row * H + vi * 8, o);
     }
     __syncthreads();  // every thread has read buffer b
     if (threadIdx.x == 0 && issued < n_mine) {
@@ -383,10 +400,10 @@ cudaError_t launch_ln_fwd(const void* X, const void* gamma, const void* beta, vo
 }
 
 cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd,
-                          const float* dXn, const void* dres, float* dX, float* part_dg,
-                          float* part_db, int64_t T, int64_t H, int shards, int blocks_per_shard,
-                          uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
-  const size_t row = static_cast<size_t>(H) * 6;
+                          const void* dXn, const void* dres, void* dX, bool bf16_grads,
+                          float* part_dg, float* part_db, int64_t T, int64_t H, int shards,
+                          int blocks_per_shard, uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
+  const size_t row = static_cast<size_t>(H) * (bf16_grads ? 4 : 6);
   const int nbuf = 2;  // two 256-thread CTAs per SM, each with a two-row ring
   const size_t smem = nbuf * row + 8 * nbuf;
   const unsigned grid = static_cast<unsigned>(shards * blocks_per_shard);
@@ -397,20 +414,24 @@ cudaError_t launch_ln_bwd(const void* X, const void* gamma, const float* mean, c
   const int64_t rps = T / shards;
   cudaError_t e = cudaSuccess;
   switch (ln_vpt(H, kLnBwdThreads)) {
-#define MLPB_LN_BWD_RES(V, R)                                                                \
-  e = set_smem(ln_bwd_kernel<V, R>, smem);                                                   \
+#define MLPB_LN_BWD_RES(V, R, B)                                                             \
+  e = set_smem(ln_bwd_kernel<V, R, B>, smem);                                                \
   if (e == cudaSuccess)                                                                      \
-    ln_bwd_kernel<V, R><<<grid, kLnBwdThreads, smem, s>>>(x, g, mean, rstd, dXn, r, dX,      \
-                                                          part_dg, part_db, rps,             \
-                                                          blocks_per_shard, Hi, nbuf, err,   \
-                                                          wait_ns);
-#define MLPB_LN_BWD(V)          \
-  case V:                       \
-    if (r != nullptr) {         \
-      MLPB_LN_BWD_RES(V, true)  \
-    } else {                    \
-      MLPB_LN_BWD_RES(V, false) \
-    }                           \
+    ln_bwd_kernel<V, R, B><<<grid, kLnBwdThreads, smem, s>>>(x, g, mean, rstd, dXn, r, dX,   \
+                                                             part_dg, part_db, rps,          \
+                                                             blocks_per_shard, Hi, nbuf,     \
+                                                             err, wait_ns);
+#define MLPB_LN_BWD(V)                 \
+  case V:                              \
+    if (r != nullptr && bf16_grads) {  \
+      MLPB_LN_BWD_RES(V, true, true)   \
+    } else if (r != nullptr) {         \
+      MLPB_LN_BWD_RES(V, true, false)  \
+    } else if (bf16_grads) {           \
+      MLPB_LN_BWD_RES(V, false, true)  \
+    } else {                           \
+      MLPB_LN_BWD_RES(V, false, false) \
+    }                                  \
     break;
     MLPB_LN_BWD(1)
     MLPB_LN_BWD(2)

@@ -4,6 +4,8 @@
 // 8 fp32 column sums (one 16-byte bf16 vector per row) over every 4th row of the split,
 // and the 4 row lanes are combined through shared memory into part[split][col].
 // Pass 2 sums the splits in a fixed order, so results are bitwise reproducible.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -72,6 +74,78 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
+// Single-launch column sums (the backward's db2 = sum_t dY): a cluster of kCsCluster CTAs
+// owns kCsCols columns and splits the rows into kCsCluster contiguous ranges.  In a CTA,
+// warp w is row lane w (rows r0 + w, r0 + w + 8, ...) and lane l owns 8 columns, so each
+// warp load reads 512 contiguous bytes of one row; kCsBatch 16-byte loads per thread are
+// issued before any is added.  The 8 row lanes are added in lane order through shared
+// memory, then the cluster's CTA 0 adds the CTAs' partial rows in rank order, reading
+// them from their shared memory (distributed shared memory), and writes (or with
+// `accumulate` adds to) out.  No second launch, no atomics: reproducible bit for bit.
+// A 16-byte streaming load (read once: no L1 allocation).  An asm volatile, so that a
+// batch of them is issued in program order before the adds that consume it.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int kCsCluster = 8;
+constexpr int kCsCols = 256;
+constexpr int kCsRowLanes = 8;
+constexpr int kCsBatch = 16;
+
+__global__ void __cluster_dims__(kCsCluster, 1, 1) __launch_bounds__(256, 2)
+    colsum_cluster_kernel(const __nv_bfloat16* __restrict__ in, int64_t R, int64_t C,
+                          float* __restrict__ out, int accumulate) {
+  __shared__ float red[kCsRowLanes][kCsCols];
+  const int lane = threadIdx.x & 31, rl = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t chunk = blockIdx.x / kCsCluster;
+  const int64_t col = chunk * kCsCols + lane * 8;
+  const int64_t rpc = (R + kCsCluster - 1) / kCsCluster;
+  const int64_t r0 = rank * rpc;
+  const int64_t r1 = min(R, r0 + rpc);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (col < C) {
+    const int64_t step = kCsRowLanes * C;  // elements between a lane's consecutive rows
+    int64_t r = r0 + rl;
+    const __nv_bfloat16* p = in + r * C + col;
+    for (; r + (kCsBatch - 1) * kCsRowLanes < r1; r += kCsBatch * kCsRowLanes) {
+      uint4 u[kCsBatch];
+#pragma unroll
+      for (int j = 0; j < kCsBatch; ++j) u[j] = ld_stream_v4(p + j * step);
+#pragma unroll
+      for (int j = 0; j < kCsBatch; ++j) add_bf16x8(u[j], acc);
+      p += kCsBatch * step;
+    }
+    for (; r < r1; r += kCsRowLanes, p += step) add_bf16x8(ld_global_nc_v4(p), acc);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rl][lane * 8 + e] = acc[e];
+  __syncthreads();
+  const int c = threadIdx.x;  // one column a thread from here on
+  float s = 0.f;
+#pragma unroll
+  for (int l = 0; l < kCsRowLanes; ++l) s += red[l][c];
+  __syncthreads();
+  red[0][c] = s;
+  cluster_sync();  // every CTA's partial row is written
+  if (rank == 0 && chunk * kCsCols + c < C) {
+    const uint32_t a = smem_u32(&red[0][c]);
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < kCsCluster; ++q) t += ld_shared_cluster_f32(mapa_shared(a, q));
+    float* o = out + chunk * kCsCols + c;
+    *o = accumulate ? *o + t : t;
+  }
+  cluster_sync();  // the peers' shared memory stays until CTA 0 has read it
+}
+
 // out[c] = sum_k part[k][c] (or out[c] += ... with `accumulate`) for one or two partial
 // arrays (blockIdx.y picks the array).
 // A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
@@ -119,6 +193,14 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
   return launch_sum_partials(part, splits, C, out, s, accumulate);
 }
 
+cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out,
+                                  cudaStream_t s, int accumulate) {
+  const unsigned chunks = static_cast<unsigned>((C + kCsCols - 1) / kCsCols);
+  colsum_cluster_kernel<<<chunks * kCsCluster, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(in), R, C, out, accumulate);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s, int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 1);
@@ -130,6 +212,32 @@ cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int n
                                  float* out_a, float* out_b, cudaStream_t s, int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 2);
   sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, part_b, nparts, C, out_a, out_b, accumulate);
+  return cudaGetLastError();
+}
+
+// dst[i] = src[i] over n16 16-byte words: the emulated sequence-parallel gathers and
+// scatters.  Grid-stride, four independent words in flight per thread.
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst,
+                                                     const uint4* __restrict__ src, size_t n16) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = ld_global_nc_v4(src + i + j * stride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) st_global_v4(dst + i + j * stride, v[j]);
+  }
+  for (; i < n16; i += stride) st_global_v4(dst + i, ld_global_nc_v4(src + i));
+}
+
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  const size_t want = (n16 + 4 * 256 - 1) / (4 * 256);
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>(want, 4 * static_cast<size_t>(num_sms)));
+  copy16_kernel<<<blocks, 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src),
+                                       n16);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "../../include/mlpb.h"
 #include "kernels.h"
@@ -21,34 +20,25 @@
 namespace {
 
 constexpr int64_t kScratchFloats = int64_t(1) << 20;  // 4 MiB of fp32 partials
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_colsum_scratch[kScratchFloats];
 
-// Device address of g_colsum_scratch and the SM count, resolved once per device.
-struct DeviceSetup {
-  float* scratch = nullptr;
-  int num_sms = 0;
-};
-DeviceSetup g_setup[kMaxDevices];
-std::mutex g_setup_mu;
-
-// Must run with `device` current.  The host-side name g_colsum_scratch is only a
-// stand-in for the device array; its device address comes from cudaGetSymbolAddress.
-mlpb_status setup_device(int device, DeviceSetup* out) {
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  DeviceSetup& s = g_setup[device];
-  if (s.scratch == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_colsum_scratch) != cudaSuccess || ptr == nullptr)
-      return MLPB_ECUDA;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-      return MLPB_ECUDA;
-    s.scratch = static_cast<float*>(ptr);
-    s.num_sms = sms;
-  }
-  *out = s;
+// The device address of g_colsum_scratch on the current device.  The host-side name
+// g_colsum_scratch is only a stand-in for the device array; its device address comes
+// from cudaGetSymbolAddress, which the first call on a device also uses to load the
+// library's device code there.  The address is resolved again on every call (a host
+// lookup once the code is loaded), so it stays valid if the caller resets the device or
+// releases and re-creates its context: a cached address could then name memory that
+// no longer holds the array.
+mlpb_status current_scratch(float** scratch, int* num_sms) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLPB_ECUDA;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_colsum_scratch) != cudaSuccess || ptr == nullptr)
+    return MLPB_ECUDA;
+  if (cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return MLPB_ECUDA;
+  *scratch = static_cast<float*>(ptr);
   return MLPB_OK;
 }
 
@@ -62,24 +52,22 @@ extern "C" mlpb_status mlpb_bias_grad_noalloc(const void* in, int64_t rows, int6
   if (cols > kScratchFloats) return MLPB_EUNSUPPORTED;  // one split of partials must fit
   if ((reinterpret_cast<uintptr_t>(in) & 15u) != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0)
     return MLPB_EINVAL;
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return MLPB_ECUDA;
-  if (device < 0 || device >= kMaxDevices) return MLPB_EUNSUPPORTED;
-  DeviceSetup setup;
-  const mlpb_status st = setup_device(device, &setup);
+  float* scratch = nullptr;
+  int num_sms = 0;
+  const mlpb_status st = current_scratch(&scratch, &num_sms);
   if (st != MLPB_OK) return st;
 
   // Row splits: about four CTAs per SM over the 512-column chunks, at least 16 rows per
   // split, and no more splits than the scratch holds.
   const int64_t chunks = (cols + 511) / 512;
-  int64_t splits = std::max<int64_t>(1, (4 * setup.num_sms + chunks - 1) / chunks);
+  int64_t splits = std::max<int64_t>(1, (4 * num_sms + chunks - 1) / chunks);
   splits = std::min<int64_t>(splits, std::max<int64_t>(1, rows / 16));
   splits = std::min<int64_t>(splits, kScratchFloats / cols);
   const int64_t rows_per_split = std::max<int64_t>(1, (rows + splits - 1) / splits);
   splits = std::max<int64_t>(1, (rows + rows_per_split - 1) / rows_per_split);
   // Pass 1 writes every partial pass 2 reads, so earlier calls' leftovers need no clearing.
   const cudaError_t e = mlpb::launch_colsum_bf16(in, rows, cols, static_cast<int>(splits),
-                                                 rows_per_split, setup.scratch, out,
+                                                 rows_per_split, scratch, out,
                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLPB_OK : MLPB_ECUDA;
 }

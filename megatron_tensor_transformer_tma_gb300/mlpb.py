@@ -29,6 +29,8 @@ MLPB_FLAG_FAULT_INJECT = 0x1
 MLPB_FLAG_ACCUMULATE_GRADS = 0x2
 MLPB_FLAG_RECOMPUTE_ACT = 0x4
 MLPB_FLAG_FP8 = 0x8
+MLPB_FLAG_BF16_OUT = 0x10
+MLPB_FLAG_EMULATE_COPIES = 0x20
 
 # Every symbol include/mlpb.h declares.
 EXPORTED = (
@@ -173,6 +175,11 @@ def mlpb_saved_size(h: Handle):
     return z.value, a.value
 
 
+def out_dtype(c):
+    """dtype of Y, dX (and the LayerNorm backward's dXn): bf16 under MLPB_FLAG_BF16_OUT."""
+    return torch.bfloat16 if c.flags & MLPB_FLAG_BF16_OUT else torch.float32
+
+
 def _w1_shape(c):
     fs = c.ffn // c.tp
     return (c.tp, 2, fs, c.hidden) if c.act == MLPB_ACT_SWIGLU else (c.tp, fs, c.hidden)
@@ -186,7 +193,7 @@ def mlpb_forward(h: Handle, X, W1, b1, W2, b2, Y, Zsaved, Asaved, workspace=None
     args = [
         _ptr(X, bf, (T, Hd), "X"), _ptr(W1, bf, _w1_shape(c), "W1"), _ptr(b1, bf, (F,), "b1"),
         _ptr(W2, bf, (t, Hd, F // t), "W2"), _ptr(b2, bf, (Hd,), "b2"),
-        _ptr(Y, torch.float32, (T, Hd), "Y"), _ptr(Zsaved, bf, (T, f1), "Zsaved"),
+        _ptr(Y, out_dtype(c), (T, Hd), "Y"), _ptr(Zsaved, bf, (T, f1), "Zsaved"),
         _ptr(Asaved, bf, (T, F), "Asaved"), _ptr(workspace, None, None, "workspace"),
     ]
     _check(load_library().mlpb_forward(h.ptr, *args, _stream(stream)), "mlpb_forward")
@@ -202,7 +209,7 @@ def mlpb_backward(h: Handle, X, W1, W2, Zsaved, Asaved, dY, dX, dW1, dW2, db1, d
         _ptr(X, bf, (T, Hd), "X"), _ptr(W1, bf, _w1_shape(c), "W1"),
         _ptr(W2, bf, (t, Hd, F // t), "W2"), _ptr(Zsaved, bf, (T, f1), "Zsaved"),
         _ptr(Asaved, bf, (T, F), "Asaved"), _ptr(dY, bf, (T, Hd), "dY"),
-        _ptr(dX, f32, (T, Hd), "dX"), _ptr(dW1, f32, _w1_shape(c), "dW1"),
+        _ptr(dX, out_dtype(c), (T, Hd), "dX"), _ptr(dW1, f32, _w1_shape(c), "dW1"),
         _ptr(dW2, f32, (t, Hd, F // t), "dW2"), _ptr(db1, f32, (F,), "db1"),
         _ptr(db2, f32, (Hd,), "db2"), _ptr(workspace, None, None, "workspace"),
     ]
@@ -227,7 +234,7 @@ def mlpb_layernorm_sp_bwd(h: Handle, X, gamma, mean, rstd, dXn, dX, dgamma, dbet
     bf, f32 = torch.bfloat16, torch.float32
     args = [_ptr(X, bf, (T, Hd), "X"), _ptr(gamma, bf, (Hd,), "gamma"),
             _ptr(mean, f32, (T,), "mean"), _ptr(rstd, f32, (T,), "rstd"),
-            _ptr(dXn, f32, (T, Hd), "dXn"), _ptr(dX, f32, (T, Hd), "dX"),
+            _ptr(dXn, out_dtype(c), (T, Hd), "dXn"), _ptr(dX, out_dtype(c), (T, Hd), "dX"),
             _ptr(dgamma, f32, (Hd,), "dgamma"), _ptr(dbeta, f32, (Hd,), "dbeta"),
             _ptr(workspace, None, None, "workspace")]
     _check(load_library().mlpb_layernorm_sp_bwd(h.ptr, *args, _stream(stream)),
@@ -244,7 +251,8 @@ def mlpb_branch_forward(h: Handle, X, gamma, beta, W1, b1, W2, b2, Y, Xn, mean, 
         _ptr(X, bf, (T, Hd), "X"), _ptr(gamma, bf, (Hd,), "gamma"), _ptr(beta, bf, (Hd,), "beta"),
         _ptr(W1, bf, _w1_shape(c), "W1"), _ptr(b1, bf, (F,), "b1"),
         _ptr(W2, bf, (t, Hd, F // t), "W2"), _ptr(b2, bf, (Hd,), "b2"),
-        _ptr(Y, f32, (T, Hd), "Y"), _ptr(Xn, bf, (T, Hd), "Xn"), _ptr(mean, f32, (T,), "mean"),
+        _ptr(Y, out_dtype(c), (T, Hd), "Y"), _ptr(Xn, bf, (T, Hd), "Xn"),
+        _ptr(mean, f32, (T,), "mean"),
         _ptr(rstd, f32, (T,), "rstd"), _ptr(Zsaved, bf, (T, f1), "Zsaved"),
         _ptr(Asaved, bf, (T, F), "Asaved"), _ptr(workspace, None, None, "workspace"),
     ]
@@ -263,7 +271,7 @@ def mlpb_branch_backward(h: Handle, X, gamma, W1, W2, Xn, mean, rstd, Zsaved, As
         _ptr(W1, bf, _w1_shape(c), "W1"), _ptr(W2, bf, (t, Hd, F // t), "W2"),
         _ptr(Xn, bf, (T, Hd), "Xn"), _ptr(mean, f32, (T,), "mean"), _ptr(rstd, f32, (T,), "rstd"),
         _ptr(Zsaved, bf, (T, f1), "Zsaved"), _ptr(Asaved, bf, (T, F), "Asaved"),
-        _ptr(dY, bf, (T, Hd), "dY"), _ptr(dX, f32, (T, Hd), "dX"),
+        _ptr(dY, bf, (T, Hd), "dY"), _ptr(dX, out_dtype(c), (T, Hd), "dX"),
         _ptr(dW1, f32, _w1_shape(c), "dW1"), _ptr(dW2, f32, (t, Hd, F // t), "dW2"),
         _ptr(db1, f32, (F,), "db1"), _ptr(db2, f32, (Hd,), "db2"),
         _ptr(dgamma, f32, (Hd,), "dgamma"), _ptr(dbeta, f32, (Hd,), "dbeta"),
@@ -316,8 +324,13 @@ def mlpb_bias_grad_noalloc(inp, out, stream=None):
     rows, cols = inp.shape
     args = [_ptr(inp, torch.bfloat16, None, "in"), rows, cols,
             _ptr(out, torch.float32, (cols,), "out")]
-    _check(load_library().mlpb_bias_grad_noalloc(*args, _stream(stream)),
-           "mlpb_bias_grad_noalloc")
+    if out.device != inp.device:
+        raise ValueError(f"in is on {inp.device} but out on {out.device}")
+    # the library picks its scratch array and SM count from the current device, and the
+    # stream must belong to that device too: make the tensors' device current
+    with torch.cuda.device(inp.device):
+        _check(load_library().mlpb_bias_grad_noalloc(*args, _stream(stream)),
+               "mlpb_bias_grad_noalloc")
 
 
 class MLPBlock:
@@ -351,7 +364,7 @@ class MLPBlock:
 
     def forward(self, X, W1, b1, W2, b2, Y=None, stream=None):
         if Y is None:
-            Y = torch.empty((self.cfg.tokens, self.cfg.hidden), dtype=torch.float32,
+            Y = torch.empty((self.cfg.tokens, self.cfg.hidden), dtype=out_dtype(self.cfg),
                             device=self.device)
         mlpb_forward(self.handle, X, W1, b1, W2, b2, Y, self.Z, self.A, self.workspace, stream)
         return Y
@@ -364,7 +377,7 @@ class MLPBlock:
         new = torch.zeros if c.flags & MLPB_FLAG_ACCUMULATE_GRADS else torch.empty
         f32 = dict(dtype=torch.float32, device=self.device)
         return dict(
-            dX=torch.empty((c.tokens, c.hidden), **f32),
+            dX=torch.empty((c.tokens, c.hidden), dtype=out_dtype(c), device=self.device),
             dW1=new(W1.shape, **f32),
             dW2=new(W2.shape, **f32),
             db1=new((c.ffn,), **f32) if has_b else None,
@@ -391,7 +404,7 @@ class MLPBranch(MLPBlock):
 
     def forward(self, X, gamma, beta, W1, b1, W2, b2, Y=None, stream=None):
         if Y is None:
-            Y = torch.empty((self.cfg.tokens, self.cfg.hidden), dtype=torch.float32,
+            Y = torch.empty((self.cfg.tokens, self.cfg.hidden), dtype=out_dtype(self.cfg),
                             device=self.device)
         mlpb_branch_forward(self.handle, X, gamma, beta, W1, b1, W2, b2, Y, self.Xn, self.mean,
                             self.rstd, self.Z, self.A, self.workspace, stream)

@@ -69,7 +69,9 @@ def test_accumulate_flag_passes_config_validation(lib):
                       (mlpb.MLPB_FLAG_ACCUMULATE_GRADS | mlpb.MLPB_FLAG_FAULT_INJECT, True),
                       (mlpb.MLPB_FLAG_RECOMPUTE_ACT, True),
                       (mlpb.MLPB_FLAG_FP8, True),
-                      (0x10, False)):
+                      (mlpb.MLPB_FLAG_BF16_OUT, True),
+                      (mlpb.MLPB_FLAG_BF16_OUT | mlpb.MLPB_FLAG_FP8, True),
+                      (0x40, False)):
         cfg = mlpb.make_config(128, 256, 1024, 2, "gelu", True, flags=flags)
         h = ctypes.c_void_p()
         st = lib.mlpb_create(ctypes.byref(cfg), ctypes.byref(h))
@@ -83,7 +85,8 @@ def test_accumulate_flag_passes_config_validation(lib):
 def test_header_flag_values_match_binding():
     src = open(os.path.join(ROOT, "include", "mlpb.h")).read()
     for name in ("MLPB_FLAG_FAULT_INJECT", "MLPB_FLAG_ACCUMULATE_GRADS",
-                 "MLPB_FLAG_RECOMPUTE_ACT", "MLPB_FLAG_FP8"):
+                 "MLPB_FLAG_RECOMPUTE_ACT", "MLPB_FLAG_FP8", "MLPB_FLAG_BF16_OUT",
+                 "MLPB_FLAG_EMULATE_COPIES"):
         m = re.search(rf"#define\s+{name}\s+(0x[0-9a-fA-F]+)u", src)
         assert m and int(m.group(1), 16) == getattr(mlpb, name), name
 

@@ -151,3 +151,12 @@ def test_job_throughput_counts_every_replica():
     assert bench.job_tflops(1e12, 1, 1000.0) == pytest.approx(1.0)
     assert bench.job_tflops(1e12, 4, 1000.0) == pytest.approx(4.0)
     assert bench.reduce_max(3.5, None, 1) == 3.5
+
+
+def test_peak_regime_follows_the_sampled_clock():
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    assert bench.peak_regime({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}, peaks) == ("burst", 1900.0)
+    assert bench.peak_regime({"sm_mhz": 1967.0, "sm_max_mhz": 2070.0}, peaks) == ("burst", 1900.0)
+    assert bench.peak_regime({"sm_mhz": 1960.0, "sm_max_mhz": 2070.0}, peaks) == \
+        ("sustained", 1700.0)
+    assert bench.peak_regime(None, peaks) == ("sustained", 1700.0)

@@ -18,7 +18,7 @@ from oracle import layernorm as oln
 from oracle import mlp as omlp
 from oracle.bf16 import round_bf16
 
-from _harness import check_full, gate, oracle_pair, run_gpu, to_f64
+from _harness import check_full, fmt_rel, gate, oracle_refs, run_gpu, to_f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -31,8 +31,8 @@ def test_reduced_tokens_every_element(wid):
     shape = reduced_tokens(WORKLOADS[wid], 512)
     d = make_inputs(shape, wid)
     gpu = run_gpu(shape, d)
-    rel = check_full(shape, gpu, oracle_pair(shape, d))
-    print(wid, {k: tuple(round(x, 5) for x in v) for k, v in rel.items()})
+    rel = check_full(shape, gpu, oracle_refs(shape, d))
+    print(wid, fmt_rel(rel))
 
 
 def _sampled_oracle(shape, f, rows, cols, store):
@@ -76,12 +76,11 @@ def test_full_tokens_sampled(wid):
     ex_r, ex_c = _sampled_oracle(shape, f, rows, cols, None)
     st_r, st_c = _sampled_oracle(shape, f, rows, cols, round_bf16)
     rel = {}
-    rel["Y"] = gate("Y", got["Y"], ex_r["Y"], st_r["Y"])
-    rel["dX"] = gate("dX", got["dX"], ex_r["dX"], st_r["dX"])
-    rel["dW2"] = gate("dW2", got["dW2"], ex_c["dW2"], st_c["dW2"])
-    rel["dW1"] = gate("dW1", got["dW1"], ex_c["dW1"], st_c["dW1"])
+    for k in ("Y", "dX"):
+        rel[k] = gate(k, got[k], ex_r[k], st_r[k])
+    for k in ("dW2", "dW1") + (("db1",) if shape.bias else ()):
+        rel[k] = gate(k, got[k], ex_c[k], st_c[k])
     if shape.bias:
-        rel["db1"] = gate("db1", got["db1"], ex_c["db1"], st_c["db1"])
         db2 = f["dY"].sum(axis=0)
         rel["db2"] = gate("db2", got["db2"], db2, db2)
-    print(wid, {k: tuple(round(x, 5) for x in v) for k, v in rel.items()})
+    print(wid, fmt_rel(rel))
