@@ -49,10 +49,18 @@
 #include "fp8.cuh"
 #include "gemm_params.h"
 
+#ifndef MLPB_DGRAD_V8
+#define MLPB_DGRAD_V8 0
+#endif
+
 namespace mlpb {
 
 template <GemmKind K>
 struct KindOf {
+  // long K (F, F1 or T): a pair's whole tiles alternate the direction of their K loop
+  static constexpr bool reverse_k = (K == GemmKind::FC2 || K == GemmKind::DX ||
+                                     K == GemmKind::WGRAD_W1 || K == GemmKind::WGRAD_W2T ||
+                                     K == GemmKind::WGRAD_W2);
   static constexpr bool a_mn = (K == GemmKind::WGRAD_W1 || K == GemmKind::WGRAD_W2T);
   static constexpr bool b_mn = (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU ||
                                 K == GemmKind::DX || K == GemmKind::WGRAD_W1 ||
@@ -139,6 +147,37 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, cons
   }
 }
 
+// The same with 32-byte accesses: two per 32 values, whole sectors (p 32-byte aligned and
+// nvalid a multiple of 16).
+__device__ __forceinline__ void load_bf16x32_v8(const __nv_bfloat16* p, int nvalid,
+                                                float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (q * 16 < nvalid) ld_global_nc_v8(p + q * 16, w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      v[q * 16 + 2 * e] = f.x;
+      v[q * 16 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+template <bool kEvictFirst = false>
+__device__ __forceinline__ void store_bf16x32_v8(__nv_bfloat16* p, int nvalid,
+                                                 const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    if (q * 16 < nvalid) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[q * 16 + 2 * e], v[q * 16 + 2 * e + 1]);
+      st_global_v8<kEvictFirst>(p + q * 16, w);
+    }
+  }
+}
+
 __device__ __forceinline__ void store_f32x32(float* p, int nvalid, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -208,15 +247,12 @@ __device__ __forceinline__ void track_amax(const float (&v)[32], int nv, float& 
     if (e < nv) am = fmaxf(am, fabsf(v[e]));
 }
 
-// Epilogue of one 128 x 256 tile for the calling thread's row, over the 32-column chunks
-// [c0, c1) of the tile (group g of kEpiGroups takes chunks [8g, 8g + 8) / kEpiGroups; the
-// SwiGLU tile's 4 gate/up chunk pairs are split the same way).  `tacc` is the TMEM address
-// of the accumulator at this warp's lane quarter.  All branches that skip tcgen05.ld are
-// uniform across the warp.
+// Epilogue of one 128 x 256 tile for the calling thread's row.  `tacc` is the TMEM
+// address of the accumulator at this warp's lane quarter.  All branches that skip
+// tcgen05.ld are uniform across the warp.
 template <GemmKind K, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, int nt,
-                                              const GemmParams& p, float sc, float& am, int grp) {
-  const int c0 = grp * (kBN / 32) / kEpiGroups, c1 = (grp + 1) * (kBN / 32) / kEpiGroups;
+                                              const GemmParams& p, float sc, float& am) {
   const int m = mt * kBM + row;
   const bool row_ok = m < p.M;
   if constexpr (K == GemmKind::FC1_GELU) {
@@ -224,7 +260,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * p.F;
     __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.F) break;
       float v[32];
@@ -252,7 +288,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F +
                        static_cast<size_t>(i) * p.Fs;
 #pragma unroll 1
-    for (int c = c0 / 2; c < c1 / 2; ++c) {
+    for (int c = 0; c < 4; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float g[32], u[32];
@@ -274,7 +310,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int n0 = nt * kBN;
     const size_t yo = static_cast<size_t>(m) * p.H;  // row m of Y (fp32, or bf16 with out_bf16)
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -308,14 +344,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     // recomputation: A = gelu(Z) from the saved Z, for the dW2 GEMM that follows
     __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + base : nullptr;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32], z[32];
       load_acc<F8>(tacc + c * 32, v, sc);
       const int nv = min(32, p.Fs - jc);
       if (row_ok) {
+#if MLPB_DGRAD_V8 & 2
+        load_bf16x32_v8(Z + jc, nv, z);
+#else
         load_bf16x32(Z + jc, nv, z);
+#endif
         if (A != nullptr) {
           float a[32];
 #pragma unroll
@@ -324,7 +364,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
+#if MLPB_DGRAD_V8 & 1
+        store_bf16x32_v8<(MLPB_DGRAD_V8 & 4) != 0>(dZ + jc, nv, v);
+#else
         store_bf16x32(dZ + jc, nv, v);
+#endif
         if constexpr (F8) track_amax(v, nv, am);
       }
       if (p.colsum != nullptr) {  // db1 partials: column sums of the stored (bf16) dZ
@@ -348,7 +392,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
                                     static_cast<size_t>(i) * p.Fs
                               : nullptr;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float da[32];
@@ -384,7 +428,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int j0 = (nt - i * p.tiles_per_shard) * kBN;
     float* dW = static_cast<float*>(p.out0) + (static_cast<size_t>(i) * p.H + m) * p.Fs;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int jc = j0 + c * 32;
       if (jc >= p.Fs) break;
       float v[32];
@@ -403,7 +447,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int j = m - i * p.Fs;
     float* dW = static_cast<float*>(p.out0) + static_cast<size_t>(i) * p.H * p.Fs + j;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -425,7 +469,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
     const int n0 = nt * kBN;
     float* dW = static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.H;
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c) {
+    for (int c = 0; c < kBN / 32; ++c) {
       const int col = n0 + c * 32;
       if (col >= p.H) break;
       float v[32];
@@ -550,7 +594,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 2 * kEpiWarps);  // every epilogue warp of both CTAs
+      mbar_init(tempty0 + 8 * b, 8);  // four epilogue warps in each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -591,9 +635,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int mp, nt;
         tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
         const int mt = mp * 2 + rank;
-        // whole tiles of odd iterations walk K backwards (kReverseK): the pair's next tile
-        // shares an operand panel with this one and starts on the k-blocks just read
-        const bool rev = kReverseK && part < 0 && (it & 1) != 0;
+        // long-K GEMMs: whole tiles of odd iterations walk K backwards.  The pair's next
+        // tile shares an operand panel with this one (the grouped raster), and it starts
+        // on the k-blocks just read, which are still in L2 (5-10 % less DRAM traffic)
+        const bool rev = KindOf<K>::reverse_k && part < 0 && (it & 1) != 0;
         bool ok = true;
         for (int i = kb0; i < kb1; ++i) {
           const int kb = rev ? kb0 + kb1 - 1 - i : i;
@@ -703,7 +748,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;  // column group: warps 2-5 group 0, warps 6-9 group 1
     const int row = quarter * 32 + lane;
     float sc = 1.0f;  // FP8: 2^-(k_a + k_b), exact
     if constexpr (F8) sc = ldexpf(1.0f, -(e4m3_scale_exp(*p.amax_a) + e4m3_scale_exp(*p.amax_b)));
@@ -729,14 +773,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    ((static_cast<size_t>(st - split_start) * split + part) * 2 + rank) * (kBM * kBN) +
                    static_cast<size_t>(row) * kBN;
 #pragma unroll 1
-        for (int c = grp * (kBN / 32) / kEpiGroups; c < (grp + 1) * (kBN / 32) / kEpiGroups;
-             ++c) {
+        for (int c = 0; c < kBN / 32; ++c) {
           float v[32];
           load_acc<F8>(tacc + c * 32, v, sc);
           store_f32x32(P + c * 32, 32, v);
         }
       } else {
-        epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am, grp);
+        epilogue_tile<K, F8>(tacc, row, mp * 2 + rank, nt, p, sc, am);
       }
       if constexpr (F8) {
         if (p.amax_out != nullptr) {  // non-negative floats order like their bit patterns

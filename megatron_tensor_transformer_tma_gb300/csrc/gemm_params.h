@@ -23,20 +23,7 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;  // k-block depth: 64 bf16 = 128-byte K-major rows (128-byte swizzle;
                          // 32-deep blocks with a 64-byte swizzle measured much slower)
 constexpr int kChunk = 64 * kBK * 2;  // one 64(MN) x kBK(K) MN-major box, 8 KB
-// Epilogue warps per CTA: 4 (one per TMEM lane quarter, each drains all 256 columns of
-// its 32 rows) or 8 (two per lane quarter, each drains 128 of the columns).
-#ifndef MLPB_EPI_WARPS
-#define MLPB_EPI_WARPS 4
-#endif
-constexpr int kEpiWarps = MLPB_EPI_WARPS;
-static_assert(kEpiWarps == 4 || kEpiWarps == 8, "4 or 8 epilogue warps");
-constexpr int kEpiGroups = kEpiWarps / 4;       // column groups of a tile
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA / relay, epilogue
-// Whole tiles of a pair's odd iterations walk their K range backwards (1) or not (0).
-#ifndef MLPB_REVERSE_K
-#define MLPB_REVERSE_K 0
-#endif
-constexpr bool kReverseK = MLPB_REVERSE_K != 0;
+constexpr int kGemmThreads = 192;  // producer, MMA / relay, four epilogue warps
 constexpr int kTmemCols = 512;
 constexpr int kClusterM = 2;  // CTAs per cluster: the pair along M
 

@@ -23,6 +23,9 @@ SMALL = [
     pytest.param(MLPShape(384, 320, 1536, 1, "gelu", False), 12, id="gelu-t1-nobias-raggedH"),
     pytest.param(MLPShape(256, 192, 704, 8, "swiglu", False), 13, id="swiglu-t8-Fs88-raggedH"),
     pytest.param(MLPShape(512, 256, 2752, 2, "swiglu", False), 14, id="swiglu-t2-Fs1376"),
+    # Fs = 160: each shard's one 256-column N tile of the SwiGLU dgrad is 96 columns of
+    # padding; 64-wide B boxes straddle the shard's end (a K-block of fc2 too)
+    pytest.param(MLPShape(256, 192, 480, 3, "swiglu", False), 19, id="swiglu-t3-Fs160-seams"),
     pytest.param(MLPShape(256, 256, 1024, 8, "gelu", True), 15, id="gelu-t8-Fs128"),
     pytest.param(MLPShape(256, 384, 1024, 4, "swiglu", False, sp_ln=True), 16, id="sp-ln-swiglu-t4"),
     pytest.param(MLPShape(128, 128, 512, 2, "gelu", True, sp_ln=True), 17, id="sp-ln-gelu-t2"),
