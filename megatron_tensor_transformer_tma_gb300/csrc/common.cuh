@@ -18,8 +18,6 @@ enum WaitSite : uint32_t {
   kSiteEpiAccFull = 4,
   kSiteDrain = 5,
   kSiteLnFull = 6,
-  kSiteRelay = 7,
-  kSitePeerFull = 8,
 };
 
 // Default limit of one bounded wait: 1 s of wall time (globaltimer).

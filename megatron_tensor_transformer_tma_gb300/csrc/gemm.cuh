@@ -6,11 +6,13 @@
 // tile, so every B byte in shared memory feeds both SMs' tensor cores.  Each CTA (192
 // threads) has:
 //   warp 0      TMA producer: a 7-stage ring of 128x64 A and 128x64 B-half bf16 tiles
-//               (128-byte swizzle, 32 KB a stage), armed with the byte count;
+//               (128-byte swizzle, 32 KB a stage).  Both CTAs' copies of a stage signal
+//               the even CTA's full barrier (the odd CTA's through .cta_group::2), which
+//               the even CTA's producer arms with both halves' byte count;
 //   warp 1      with its peer, allocates 512 TMEM columns (two 256-column fp32
-//               accumulators); in the even CTA it issues the pair's tcgen05.mma (M=256,
-//               N=256, K=16) and commits each consumed stage to both CTAs' producers; in
-//               the odd CTA it relays "this stage has landed here" to the even CTA;
+//               accumulators); in the even CTA it waits on that one barrier, issues the
+//               pair's tcgen05.mma (M=256, N=256, K=16) and commits each consumed stage to
+//               both CTAs' producers;
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows (each warp owns the
 //               32 TMEM lanes of its warp-id modulo 4), the fused pointwise op, stores to
 //               HBM, then the accumulator is released to the even CTA's MMA issuer.
@@ -51,6 +53,15 @@
 
 #ifndef MLPB_DGRAD_V8
 #define MLPB_DGRAD_V8 0
+#endif
+#ifndef MLPB_FC1_V8
+#define MLPB_FC1_V8 0
+#endif
+#ifndef MLPB_F32_V8
+#define MLPB_F32_V8 0
+#endif
+#ifndef MLPB_EPI_SLEEP
+#define MLPB_EPI_SLEEP 0
 #endif
 
 namespace mlpb {
@@ -179,6 +190,20 @@ __device__ __forceinline__ void store_bf16x32_v8(__nv_bfloat16* p, int nvalid,
 }
 
 __device__ __forceinline__ void store_f32x32(float* p, int nvalid, const float (&v)[32]) {
+#if MLPB_F32_V8
+  if ((nvalid & 7) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q * 8 < nvalid) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[q * 8 + e]);
+        st_global_v8(p + q * 8, w);
+      }
+    }
+    return;
+  }
+#endif
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     if (q * 4 < nvalid) {
@@ -272,11 +297,19 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] += b[e];
       }
+#if MLPB_FC1_V8
+      if (row_ok) store_bf16x32_v8(Z + col, nv, v);
+#else
       if (row_ok) store_bf16x32(Z + col, nv, v);
+#endif
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
       if (row_ok) {
+#if MLPB_FC1_V8
+        store_bf16x32_v8(A + col, nv, v);
+#else
         store_bf16x32(A + col, nv, v);
+#endif
         if constexpr (F8) track_amax(v, nv, am);
       }
     }
@@ -380,6 +413,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         if (lane < nv)
           p.colsum[static_cast<size_t>(m >> 5) * p.F + static_cast<size_t>(i) * p.Fs + jc + lane] = cs;
       }
+#if MLPB_EPI_SLEEP
+      __nanosleep(MLPB_EPI_SLEEP);
+#endif
     }
   } else if constexpr (K == GemmKind::DGRAD_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
@@ -483,6 +519,29 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
   }
 }
 
+// A stage's TMA loads land in the issuing CTA's shared memory.  The even CTA's signal its
+// own full barrier; the odd CTA's (kPeer) signal the even CTA's, through .cta_group::2, so
+// the pair's MMA issuer waits on one barrier for both halves of a stage.
+template <bool kPeer>
+__device__ __forceinline__ void ld2(uint32_t d, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+  if constexpr (kPeer) tma_load_2d_pair(d, m, bar, c0, c1);
+  else tma_load_2d(d, m, bar, c0, c1);
+}
+
+template <bool kPeer>
+__device__ __forceinline__ void ld3(uint32_t d, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                    int c2) {
+  if constexpr (kPeer) tma_load_3d_pair(d, m, bar, c0, c1, c2);
+  else tma_load_3d(d, m, bar, c0, c1, c2);
+}
+
+template <bool kPeer>
+__device__ __forceinline__ void ld4(uint32_t d, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                    int c2, int c3) {
+  if constexpr (kPeer) tma_load_4d_pair(d, m, bar, c0, c1, c2, c3);
+  else tma_load_4d(d, m, bar, c0, c1, c2, c3);
+}
+
 // One stage of one CTA of the pair: its own 128 A rows, and its 128-row half of B (K-major:
 // one box; MN-major: two 64-wide chunks).
 // FP8: every operand is K-major (E4M3 copies, transposed where needed), one box each:
@@ -492,34 +551,34 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 //   DX   A dZq [T][F1]          B W1t [H][F1]
 //   WGRAD_W2 A dYt [H][T]       B At [t][Fs][T]
 //   WGRAD_W1 A dZt [F1][T]      B Xt [H][T]
-template <GemmKind K>
+template <GemmKind K, bool kPeer>
 __device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUtensorMap* tB,
                                                uint32_t sa, uint32_t sb, uint32_t bar, int mt,
                                                int nt, int kb, int rank, const GemmParams& p) {
   const int k0 = kb * kBK8;
   const int nh = nt * kBN + 128 * rank;
   if constexpr (K == GemmKind::FC1_GELU || K == GemmKind::DX || K == GemmKind::WGRAD_W1) {
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_2d(sb, tB, bar, k0, nh);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    ld2<kPeer>(sb, tB, bar, k0, nh);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * 128;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_4d(sb, tB, bar, k0, j0, rank, i);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    ld4<kPeer>(sb, tB, bar, k0, j0, rank, i);
   } else if constexpr (K == GemmKind::FC2) {
     const int i = kb / p.kb_per_shard;
     const int j0 = (kb - i * p.kb_per_shard) * kBK8;
-    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
-    tma_load_3d(sb, tB, bar, j0, nh, i);
+    ld3<kPeer>(sa, tA, bar, j0, mt * kBM, i);
+    ld3<kPeer>(sb, tB, bar, j0, nh, i);
   } else {  // DGRAD_*, WGRAD_W2: B rows are shard i's rows j0.. of a [t][Fs][K] operand
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_3d(sb, tB, bar, k0, j0, i);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    ld3<kPeer>(sb, tB, bar, k0, j0, i);
   }
 }
 
-template <GemmKind K>
+template <GemmKind K, bool kPeer>
 __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CUtensorMap* tB,
                                                  uint32_t sa, uint32_t sb, uint32_t bar, int mt,
                                                  int nt, int kb, int rank,
@@ -528,33 +587,35 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
   const int k0 = kb * kBK;
   const int nh = nt * kBN + 128 * rank;  // first B row (N index) of this CTA's half
   if constexpr (K == GemmKind::FC1_GELU) {
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_2d(sb, tB, bar, k0, nh);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    ld2<kPeer>(sb, tB, bar, k0, nh);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
+    // W1 as [2F][H]: shard i's gate rows (even CTA) or up rows (odd CTA) j0..
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * 128;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
-    tma_load_4d(sb, tB, bar, k0, j0, rank, i);  // even CTA: gate rows, odd CTA: up rows
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    ld2<kPeer>(sb, tB, bar, k0, (2 * i + rank) * p.Fs + j0);
   } else if constexpr (K == GemmKind::FC2) {
+    // K walks the shards: A [T][F] at shard i's columns, W2 as [tH][Fs] at shard i's rows
     const int i = kb / p.kb_per_shard;
     const int j0 = (kb - i * p.kb_per_shard) * kBK;
-    tma_load_3d(sa, tA, bar, j0, mt * kBM, i);
-    tma_load_3d(sb, tB, bar, j0, nh, i);
+    ld2<kPeer>(sa, tA, bar, i * p.Fs + j0, mt * kBM);
+    ld2<kPeer>(sb, tB, bar, j0, i * p.H + nh);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_3d(sb + q * kChunk, tB, bar, j0 + 64 * q, k0, i);
+    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, j0 + 64 * q, i * p.H + k0);
   } else if constexpr (K == GemmKind::DX) {
-    tma_load_2d(sa, tA, bar, k0, mt * kBM);
+    ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
   } else {  // WGRAD_W1, WGRAD_W2T
 #pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+    for (int q = 0; q < 2; ++q) ld2<kPeer>(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) tma_load_2d(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
   }
 }
 
@@ -570,14 +631,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + S * kPairAStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  const uint32_t full0 = smem_u32(bars);            // this CTA's TMA landed
-  const uint32_t pfull0 = smem_u32(bars + S);       // even CTA: the odd CTA's TMA landed
-  const uint32_t empty0 = smem_u32(bars + 2 * S);   // the pair's MMAs have read stage s
-  const uint32_t tfull0 = smem_u32(bars + 3 * S);
-  const uint32_t tempty0 = smem_u32(bars + 3 * S + 2);
-  const uint32_t drain = smem_u32(bars + 3 * S + 4);
+  const uint32_t full0 = smem_u32(bars);            // even CTA: both CTAs' halves of stage s landed
+  const uint32_t empty0 = smem_u32(bars + S);       // the pair's MMAs have read stage s
+  const uint32_t tfull0 = smem_u32(bars + 2 * S);
+  const uint32_t tempty0 = smem_u32(bars + 2 * S + 2);
+  const uint32_t drain = smem_u32(bars + 2 * S + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -588,8 +648,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(pfull0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 1);  // the even CTA's producer arms it for both halves
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -611,7 +670,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   cluster_sync();  // both CTAs' barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t pfull_lead = mapa_shared(pfull0, 0);
+  const uint32_t full_lead = mapa_shared(full0, 0);
   const uint32_t tempty_lead = mapa_shared(tempty0, 0);
 
   const WaitCtx wc{abort_flag, p.err, p.wait_ns};
@@ -646,19 +705,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          const uint32_t sa = sA0 + stage * kPairAStage, sb = sB0 + stage * kPairBStage;
           if (skip_once) {
             skip_once = false;  // fault injection: this stage is never armed
-          } else {
+          } else if (leader) {
+            // one arrival with both CTAs' bytes; the odd CTA's copies may land first (the
+            // barrier's transaction count goes below zero until this expect-tx)
             const uint32_t fb = full0 + 8 * stage;
-            mbar_arrive_expect_tx(fb, kPairStageBytes);
+            mbar_arrive_expect_tx(fb, 2 * kPairStageBytes);
             if constexpr (F8)
-              issue_stage_f8<K>(&tmA, &tmB, sA0 + stage * kPairAStage, sB0 + stage * kPairBStage,
-                                fb, mt, nt, kb, rank, p);
+              issue_stage_f8<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
             else
-              issue_stage_pair<K>(&tmA, &tmB, sA0 + stage * kPairAStage,
-                                  sB0 + stage * kPairBStage, fb, mt, nt, kb, rank, p);
+              issue_stage_pair<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          } else {
+            const uint32_t fb = full_lead + 8 * stage;
+            if constexpr (F8)
+              issue_stage_f8<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+            else
+              issue_stage_pair<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+            armed = 1u;  // issued copies that nothing in this CTA observes
           }
           if (++stage == S) {
             stage = 0;
@@ -667,8 +734,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) break;
       }
-      for (int s = 0; s < S; ++s)
-        if (armed & (1u << s)) wait_drain(full0 + 8 * s, (armed_par >> s) & 1u, wc);
+      if (leader) {
+        // every armed stage's bytes, the odd CTA's included, have landed
+        for (int s = 0; s < S; ++s)
+          if (armed & (1u << s)) wait_drain(full0 + 8 * s, (armed_par >> s) & 1u, wc);
+      } else if (armed != 0u && *abort_flag) {
+        // The odd CTA's copies signal the even CTA's barriers.  Without an abort every copy
+        // it issued is consumed by an MMA that waited for it before the final cluster
+        // barrier.  After one, its last copies were issued before a bounded wait expired
+        // (a second at the default limit) and have long landed; settle a little longer
+        // before the shared memory they write can be released.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 20000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -691,8 +770,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d = tmem_base + buf * kBN;
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {  // stage order; the producer chose the k-blocks
-          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull) ||
-              !wait_bounded(pfull0 + 8 * stage, phase, wc, kSitePeerFull)) {
+          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteMmaFull)) {
             ok = false;
             break;
           }
@@ -723,27 +801,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       umma_commit_pair(drain);
       wait_drain(drain, 0, wc);
-    } else if (lane == 0) {
-      // ---------------------------------------------------------------- relay (odd CTA)
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int u = cid; u < num_units; u += nclusters) {
-        int st, kb0, kb1, part;
-        unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bounded(full0 + 8 * stage, phase, wc, kSiteRelay)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_remote(pfull_lead + 8 * stage);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-      }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
