@@ -110,23 +110,32 @@ __device__ __forceinline__ void unit_range(int u, int split, int split_start, in
 }
 
 // ------------------------------------------------------------------ pointwise math
-// tanh-form GELU written as z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), which is
-// the same function (1 + tanh(u) = 2 sigmoid(2u)) without cancellation for z << 0.
+// tanh-form GELU written with s = sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3): since
+// 1 + tanh(u) = 2 sigmoid(2u), gelu(z) = z s, the same function without cancellation for
+// z << 0, and gelu'(z) = s + z s (1 - s) 2 sqrt(2/pi) (1 + 3 * 0.044715 z^2).  The
+// constants are folded so that e^{-2u} is one exponential of z (a + b z^2):
+//   e^{-2u} = exp(z (-2k - 2k c z^2)),  k = sqrt(2/pi), c = 0.044715.
+// For |z| past ~10 the exponential overflows to +inf (s = 0) or underflows to 0 (s = 1),
+// and both forms then return their limits (0 and z; 0 and 1) with no inf * 0.
 constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kGeluCubic = 0.044715f;
+constexpr float kGeluA = -2.0f * kSqrt2OverPi;                 // -2k
+constexpr float kGeluB = -2.0f * kSqrt2OverPi * kGeluCubic;    // -2kc
+constexpr float kGeluD0 = 2.0f * kSqrt2OverPi;                 // 2k
+constexpr float kGeluD2 = 6.0f * kSqrt2OverPi * kGeluCubic;    // 6kc
 
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float gelu_f(float z) {
-  const float u = kSqrt2OverPi * (z + kGeluCubic * z * z * z);
-  return z * sigmoid_f(2.0f * u);
+  const float t = __expf(z * fmaf(kGeluB, z * z, kGeluA));  // e^{-2u}
+  return z * __fdividef(1.0f, 1.0f + t);
 }
 
 __device__ __forceinline__ float gelu_grad_f(float z) {
   const float z2 = z * z;
-  const float u = kSqrt2OverPi * (z + kGeluCubic * z2 * z);
-  const float s = sigmoid_f(2.0f * u);
-  return s + 2.0f * z * s * (1.0f - s) * kSqrt2OverPi * (1.0f + 3.0f * kGeluCubic * z2);
+  const float s = __fdividef(1.0f, 1.0f + __expf(z * fmaf(kGeluB, z2, kGeluA)));
+  const float d = z * fmaf(kGeluD2, z2, kGeluD0);  // 2k z (1 + 3c z^2)
+  return fmaf(d, fmaf(-s, s, s), s);               // s + d s (1 - s)
 }
 
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid, float (&v)[32]) {
