@@ -74,6 +74,9 @@ def parse():
                    help="accumulate parameter gradients into fp32 main-grad buffers")
     p.add_argument("--bf16-out", action="store_true",
                    help="Y and dX (and the LayerNorm backward's dXn, dX) stored as bf16")
+    p.add_argument("--emulate-copies", action="store_true",
+                   help="the sequence-parallel gathers and scatters as device copies "
+                        "(sequence-parallel workloads)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--no-extra", action="store_true",
@@ -102,7 +105,7 @@ def kernel_source_hash():
 
 
 def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=False,
-              bf16_out=False):
+              bf16_out=False, emulate_copies=False):
     return {"workload": (shape.name or f"workload {wid}") + (" + residual" if branch else ""),
             "tokens": shape.tokens,
             "hidden": shape.hidden, "ffn": shape.ffn, "tp_emulated": shape.tp,
@@ -111,6 +114,7 @@ def config_of(shape, wid, grad_accum=False, branch=False, recompute=False, fp8=F
             "recompute_act": bool(recompute),
             "gemm_operands": "e4m3 (per-tensor power-of-two scales)" if fp8 else "bf16",
             "y_dx_dtype": "bf16" if bf16_out else "fp32",
+            "sp_exchange": "device copies" if emulate_copies else "row-block views",
             "parallelism": "emulated TP inside one GPU; replicas across GPUs",
             "l2": "inputs larger than L2 (no flush needed)"}
 
@@ -522,6 +526,10 @@ def run_native(args, rank, world, local_rank):
         flags |= mlpb.MLPB_FLAG_FP8
     if args.bf16_out:
         flags |= mlpb.MLPB_FLAG_BF16_OUT
+    if args.emulate_copies:
+        if not shape.sp_ln:
+            raise SystemExit("--emulate-copies needs a workload with the sequence-parallel layout")
+        flags |= mlpb.MLPB_FLAG_EMULATE_COPIES
     if args.branch:
         blk = mlpb.MLPBranch(shape.tokens, shape.hidden, shape.ffn, shape.tp, shape.act,
                              shape.bias, shape.ln_eps, flags)
@@ -656,7 +664,8 @@ def run_native(args, rank, world, local_rank):
         roofline = {"bound": "hbm", "kernel": top["name"], "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"{peak_src} copy"}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
-    plain = not (args.grad_accum or args.branch or args.recompute or args.bf16_out)
+    plain = not (args.grad_accum or args.branch or args.recompute or args.bf16_out or
+                 args.emulate_copies)
     roofline["traffic"] = recorded_traffic(top["name"], args.workload, shape) if plain else None
 
     # ---- e2e: the same step from pinned host buffers, outputs read back every step
@@ -678,7 +687,7 @@ def run_native(args, rank, world, local_rank):
                "dtype": "e4m3" if args.fp8 else "bf16",
                "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
                "config": config_of(shape, args.workload, args.grad_accum, args.branch,
-                                   args.recompute, args.fp8, args.bf16_out),
+                                   args.recompute, args.fp8, args.bf16_out, args.emulate_copies),
                "frac_of_dense_bf16_peak": value / world / bf16_peak,
                "frac_of_burst_peak": value / world / peaks["bf16_tflops"],
                "frac_of_sustained_peak": value / world / peaks["bf16_tflops_sustained"],

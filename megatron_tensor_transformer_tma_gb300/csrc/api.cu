@@ -794,7 +794,7 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
   // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
   if (bias) {
     LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
-    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, s2, acc);
+    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, h->num_sms, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -941,7 +941,7 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
   }
   if (st == MLPB_OK && bias) {  // db2 = sum_t dY on the bf16 dY
     LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
-    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, s, acc);
+    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, h->num_sms, s, acc);
     lt.done();
     st = from_cuda(e);
   }

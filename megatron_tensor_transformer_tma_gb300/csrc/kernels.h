@@ -35,9 +35,9 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int accumulate = 0);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s, int accumulate = 0);
-// reduce.cu: the same column sums in one launch (clusters of 8 CTAs reduce through
-// distributed shared memory); C % 8 == 0, no scratch.
-cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out,
+// reduce.cu: the same column sums in one launch (clusters of up to 8 CTAs, one an SM,
+// reduce through distributed shared memory); C % 8 == 0, no scratch.
+cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out, int num_sms,
                                   cudaStream_t s, int accumulate = 0);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,

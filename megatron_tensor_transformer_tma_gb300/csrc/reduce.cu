@@ -74,14 +74,15 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
-// Single-launch column sums (the backward's db2 = sum_t dY): a cluster of kCsCluster CTAs
-// owns kCsCols columns and splits the rows into kCsCluster contiguous ranges.  In a CTA,
-// warp w is row lane w (rows r0 + w, r0 + w + 8, ...) and lane l owns 8 columns, so each
-// warp load reads 512 contiguous bytes of one row; kCsBatch 16-byte loads per thread are
-// issued before any is added.  The 8 row lanes are added in lane order through shared
-// memory, then the cluster's CTA 0 adds the CTAs' partial rows in rank order, reading
-// them from their shared memory (distributed shared memory), and writes (or with
-// `accumulate` adds to) out.  No second launch, no atomics: reproducible bit for bit.
+// Single-launch column sums (the backward's db2 = sum_t dY): a cluster of `cs` CTAs (cs <=
+// 8, at most one CTA an SM: the launcher picks the largest cs with chunks x cs <= SMs)
+// owns kCsCols columns and splits the rows into cs contiguous ranges.  In a CTA, warp w
+// reads rows w, w + 8, ... (each warp load is 512 contiguous bytes of one row) and lane l
+// keeps 8 columns; kCsBatch 16-byte loads per thread are issued before any is added.  The
+// 8 row lanes are added in lane order through shared memory, then the cluster's CTA 0
+// adds the CTAs' partial rows in rank order, reading them from their shared memory
+// (distributed shared memory), and writes (or with `accumulate` adds to) out.  No second
+// launch, no atomics: reproducible bit for bit.
 // A 16-byte streaming load (read once: no L1 allocation).  An asm volatile, so that a
 // batch of them is issued in program order before the adds that consume it.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -92,20 +93,21 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
-constexpr int kCsCluster = 8;
+constexpr int kCsMaxCluster = 8;
 constexpr int kCsCols = 256;
 constexpr int kCsRowLanes = 8;
-constexpr int kCsBatch = 16;
+constexpr int kCsBatch = 24;
 
-__global__ void __cluster_dims__(kCsCluster, 1, 1) __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 1)
     colsum_cluster_kernel(const __nv_bfloat16* __restrict__ in, int64_t R, int64_t C,
                           float* __restrict__ out, int accumulate) {
   __shared__ float red[kCsRowLanes][kCsCols];
   const int lane = threadIdx.x & 31, rl = threadIdx.x >> 5;
   const uint32_t rank = cluster_ctarank();
-  const int64_t chunk = blockIdx.x / kCsCluster;
+  const uint32_t cs = cluster_nctarank();
+  const int64_t chunk = blockIdx.x / cs;
   const int64_t col = chunk * kCsCols + lane * 8;
-  const int64_t rpc = (R + kCsCluster - 1) / kCsCluster;
+  const int64_t rpc = (R + cs - 1) / cs;
   const int64_t r0 = rank * rpc;
   const int64_t r1 = min(R, r0 + rpc);
   float acc[8];
@@ -138,8 +140,7 @@ __global__ void __cluster_dims__(kCsCluster, 1, 1) __launch_bounds__(256, 2)
   if (rank == 0 && chunk * kCsCols + c < C) {
     const uint32_t a = smem_u32(&red[0][c]);
     float t = 0.f;
-#pragma unroll
-    for (int q = 0; q < kCsCluster; ++q) t += ld_shared_cluster_f32(mapa_shared(a, q));
+    for (uint32_t q = 0; q < cs; ++q) t += ld_shared_cluster_f32(mapa_shared(a, q));
     float* o = out + chunk * kCsCols + c;
     *o = accumulate ? *o + t : t;
   }
@@ -193,12 +194,24 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
   return launch_sum_partials(part, splits, C, out, s, accumulate);
 }
 
-cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out,
+cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out, int num_sms,
                                   cudaStream_t s, int accumulate) {
-  const unsigned chunks = static_cast<unsigned>((C + kCsCols - 1) / kCsCols);
-  colsum_cluster_kernel<<<chunks * kCsCluster, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(in), R, C, out, accumulate);
-  return cudaGetLastError();
+  const int64_t chunks = (C + kCsCols - 1) / kCsCols;
+  const int cs = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(kCsMaxCluster, num_sms / std::max<int64_t>(1, chunks))));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(chunks * cs), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, colsum_cluster_kernel, static_cast<const __nv_bfloat16*>(in),
+                            R, C, out, accumulate);
 }
 
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
