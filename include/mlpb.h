@@ -169,7 +169,8 @@ void mlpb_destroy(mlpb_handle *h);
 
 /* Bytes of device scratch the caller passes as `workspace` to mlpb_forward,
  * mlpb_backward and mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16, with a bias the
- * db1 column sums of each 32-row group of dZ that the dgrad epilogue writes, two regions of fp32 partial tiles for the K-range split of a GEMM's last
+ * db1 column sums of each 32-row group of dZ that the dgrad epilogue writes, a transposed
+ * copy of W2 ([F][H] bf16, the dgrad GEMM's operand; not under MLPB_FLAG_FP8), two regions of fp32 partial tiles for the K-range split of a GEMM's last
  * wave -- dX and dW1 run at once on two streams -- and, under MLPB_FLAG_FP8, the
  * E4M3 operand copies and their amax words). */
 mlpb_status mlpb_workspace_size(const mlpb_handle *h, size_t *bytes);

@@ -284,7 +284,15 @@ size_t ws_split_region(const mlpb_handle* h) {
 
 size_t ws_split_bytes(const mlpb_handle* h) { return 2 * ws_split_region(h); }
 
-size_t ws_backward_bytes(const mlpb_handle* h) { return ws_split_offset(h) + ws_split_bytes(h); }
+// The bf16 backward's transposed copy of W2 ([F][H] bf16, the dgrad GEMM's K-major B),
+// after the split regions.
+size_t ws_w2t_offset(const mlpb_handle* h) { return ws_split_offset(h) + ws_split_bytes(h); }
+
+size_t ws_w2t_bytes(const mlpb_handle* h) {
+  return h->fp8 ? 0 : align256(static_cast<size_t>(h->F * h->H * 2));
+}
+
+size_t ws_backward_bytes(const mlpb_handle* h) { return ws_w2t_offset(h) + ws_w2t_bytes(h); }
 
 float* ws_split_partial(const mlpb_handle* h, void* workspace, int region = 0) {
   return workspace == nullptr
@@ -772,10 +780,12 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
 
   // Tensor maps of all four GEMMs first: an encoding error launches nothing.
   CUtensorMap tdgA, tdgB, tw2A, tw2B, tw1A, tw1B, tdxA, tdxB;
+  void* w2t = ws + ws_w2t_offset(h);
   {
-    // W2 [t][H][Fs] as the 2-D [tH][Fs] (MN-major B of the dgrad: 64 columns j of shard i's
-    // rows k; j past Fs reads zeros)
-    if (!map2d(&tdgA, dY, H, T, H, kBK, kBM) || !map2d(&tdgB, W2, Fs, t * H, Fs, 64, kBK) ||
+    // the dgrad's B is W2's per-shard transpose [F][H] (K-major rows i Fs + j), written by
+    // the transpose below; a 128-row box past shard i's Fs rows reads the next shard's
+    // rows, which land in output columns the epilogue drops
+    if (!map2d(&tdgA, dY, H, T, H, kBK, kBM) || !map2d(&tdgB, w2t, H, F, H, kBK, kBN / 2) ||
         !map2d(&tw2A, Asaved, F, T, F, 64, kBK) || !map2d(&tw2B, dY, H, T, H, 64, kBK) ||
         !map2d(&tw1A, dZ, F1, T, F1, 64, kBK) || !map2d(&tw1B, X, H, T, H, 64, kBK) ||
         !map2d(&tdxA, dZ, F1, T, F1, kBK, kBM) || !map2d(&tdxB, W1, H, F1, H, 64, kBK))
@@ -795,6 +805,14 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
   if (bias) {
     LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
     cudaError_t e = launch_colsum_cluster(dY, T, H, db2, h->num_sms, s2, acc);
+    lt.done();
+    st = from_cuda(e);
+  }
+
+  // ---- [s] W2's per-shard transpose for the dgrad (K-major B), beside db2
+  if (st == MLPB_OK) {
+    LaunchTimer lt(h, s, "w2_transpose", 0.0, 4.0 * F * H);
+    cudaError_t e = launch_transpose_w2(W2, w2t, static_cast<int>(t), H, Fs, s);
     lt.done();
     st = from_cuda(e);
   }

@@ -34,8 +34,9 @@
 //   FC1_SWIGLU    [G|U] = X [Wg_i|Wu_i]^T, A = silu(G)U  (per shard i, 128 gate + 128 up
 //                 columns per tile: the even CTA holds the gate rows, the odd the up rows)
 //   FC2           Y = sum_i A_i W2_i^T + b2 (+ R)     M=T  N=H      K=t x Fs (walks shards)
-//   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B MN-major
-//   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B MN-major
+//   DGRAD_GELU    dZ = (dY W2) * gelu'(Z)             M=T  N=F      K=H   B = W2's
+//                 per-shard transpose [F][H] (K-major; a copy the backward makes first)
+//   DGRAD_SWIGLU  dG = dA U silu'(G), dU = dA silu(G) M=T  N=F      K=H   B as DGRAD_GELU
 //                 (both may also rewrite A = act(saved Z) for dW2: recomputation)
 //   DX            dX = sum_i dZ_i W1_i                M=T  N=H      K=F1  B MN-major
 //   WGRAD_W2T     dW2_i^T = A_i^T dY                  M=F  N=H      K=T   A,B MN-major
@@ -73,8 +74,7 @@ struct KindOf {
                                      K == GemmKind::WGRAD_W1 || K == GemmKind::WGRAD_W2T ||
                                      K == GemmKind::WGRAD_W2);
   static constexpr bool a_mn = (K == GemmKind::WGRAD_W1 || K == GemmKind::WGRAD_W2T);
-  static constexpr bool b_mn = (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU ||
-                                K == GemmKind::DX || K == GemmKind::WGRAD_W1 ||
+  static constexpr bool b_mn = (K == GemmKind::DX || K == GemmKind::WGRAD_W1 ||
                                 K == GemmKind::WGRAD_W2T);
 };
 
@@ -611,11 +611,11 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
     ld2<kPeer>(sa, tA, bar, i * p.Fs + j0, mt * kBM);
     ld2<kPeer>(sb, tB, bar, j0, i * p.H + nh);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
+    // B = W2's transposed copy [F][H]: shard i's rows j0.. (K-major)
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, j0 + 64 * q, i * p.H + k0);
+    ld2<kPeer>(sb, tB, bar, k0, i * p.Fs + j0);
   } else if constexpr (K == GemmKind::DX) {
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
 #pragma unroll

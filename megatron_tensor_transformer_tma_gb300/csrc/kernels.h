@@ -43,6 +43,10 @@ cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* o
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
                                  float* out_a, float* out_b, cudaStream_t s, int accumulate = 0);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
+// reduce.cu: W2 [t][H][Fs] bf16 -> its per-shard transpose W2t [t][Fs][H] (= [F][H]);
+// H % 64 == 0, Fs % 8 == 0.
+cudaError_t launch_transpose_w2(const void* w2, void* w2t, int t, int64_t H, int64_t Fs,
+                                cudaStream_t s);
 // reduce.cu: a device copy of `bytes` (a multiple of 16, both pointers 16-byte aligned).
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s);
 

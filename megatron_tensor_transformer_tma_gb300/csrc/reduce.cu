@@ -228,6 +228,65 @@ cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int n
   return cudaGetLastError();
 }
 
+// W2t[i][j][h] = W2[i][h][j]: each shard's [H][Fs] slice of W2 transposed into the rows
+// i Fs + j of a K-major [F][H] copy, which the dgrad GEMM reads as its B operand (read
+// column-wise from W2 itself, as an MN-major operand, the GEMM measured 7 % slower).  A CTA
+// moves a 64 (h) x 128 (j) tile: eight lanes load each 128-byte run of a W2 row, and eight
+// lanes store each 128-byte run of a W2t row, so both sides move whole lines.
+// H % 64 == 0, Fs % 8 == 0.
+__global__ void __launch_bounds__(256) transpose_w2_kernel(const __nv_bfloat16* __restrict__ w2,
+                                                          __nv_bfloat16* __restrict__ w2t,
+                                                          int H, int Fs) {
+  // Shared memory holds the tile transposed as 32-bit words, each the pair (h, h + 1) at
+  // one f: row f of 32 words (+1 of padding) is the 128-byte run of row f of the copy.
+  __shared__ uint32_t tileT[128][33];
+  const int i = blockIdx.z;
+  const int h0 = blockIdx.y * 64, f0 = blockIdx.x * 128;
+  const int c8 = threadIdx.x & 7, p = threadIdx.x >> 3;  // f chunk of 8, h pair
+  const __nv_bfloat16* src = w2 + (static_cast<size_t>(i) * H + h0 + 2 * p) * Fs + f0;
+  uint4 u[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {  // both f halves, rows 2p and 2p + 1: four loads in flight
+    const int c = (c8 + 8 * q) * 8;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      u[q][r] = f0 + c < Fs ? ld_global_nc_v4(src + static_cast<size_t>(r) * Fs + c)
+                            : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t lo[4] = {u[q][0].x, u[q][0].y, u[q][0].z, u[q][0].w};
+    const uint32_t hi[4] = {u[q][1].x, u[q][1].y, u[q][1].z, u[q][1].w};
+    const int f = (c8 + 8 * q) * 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {  // columns f + 2e and f + 2e + 1 of rows 2p, 2p + 1
+      tileT[f + 2 * e][p] = (lo[e] & 0xffffu) | (hi[e] << 16);
+      tileT[f + 2 * e + 1][p] = (lo[e] >> 16) | (hi[e] & 0xffff0000u);
+    }
+  }
+  __syncthreads();
+  // eight lanes write one 128-byte row of the copy: whole lines, no partial sectors
+  const int k = threadIdx.x & 7;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int f = (threadIdx.x >> 3) + 32 * r;
+    if (f0 + f >= Fs) break;
+    const uint4 v = make_uint4(tileT[f][4 * k], tileT[f][4 * k + 1], tileT[f][4 * k + 2],
+                               tileT[f][4 * k + 3]);
+    st_global_v4(w2t + (static_cast<size_t>(i) * Fs + f0 + f) * H + h0 + 8 * k, v);
+  }
+}
+
+cudaError_t launch_transpose_w2(const void* w2, void* w2t, int t, int64_t H, int64_t Fs,
+                                cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((Fs + 127) / 128), static_cast<unsigned>(H / 64),
+                  static_cast<unsigned>(t));
+  transpose_w2_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w2),
+                                           static_cast<__nv_bfloat16*>(w2t), static_cast<int>(H),
+                                           static_cast<int>(Fs));
+  return cudaGetLastError();
+}
+
 // dst[i] = src[i] over n16 16-byte words: the emulated sequence-parallel gathers and
 // scatters.  Grid-stride, four independent words in flight per thread.
 __global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst,
