@@ -783,8 +783,8 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
   void* w2t = ws + ws_w2t_offset(h);
   {
     // the dgrad's B is W2's per-shard transpose [F][H] (K-major rows i Fs + j), written by
-    // the transpose below; a 128-row box past shard i's Fs rows reads the next shard's
-    // rows, which land in output columns the epilogue drops
+    // the transpose below; with N tiles per shard, a 128-row box past shard i's Fs rows
+    // reads the next shard's rows, which land in output columns the epilogue drops
     if (!map2d(&tdgA, dY, H, T, H, kBK, kBM) || !map2d(&tdgB, w2t, H, F, H, kBK, kBN / 2) ||
         !map2d(&tw2A, Asaved, F, T, F, 64, kBK) || !map2d(&tw2B, dY, H, T, H, 64, kBK) ||
         !map2d(&tw1A, dZ, F1, T, F1, 64, kBK) || !map2d(&tw1B, X, H, T, H, 64, kBK) ||
@@ -822,8 +822,13 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
     GemmParams p = base_params(h);
     p.M = static_cast<int>(T);
     p.num_m_tiles = static_cast<int>(T / kBM);
+    // N tiles over all F columns, across shard seams (no shard pads its last tile), when
+    // every 32-column chunk of a tile lies in one shard's block of the saved activations:
+    // always for GELU ([T][F] layouts), for SwiGLU ([T][2F], a gate and an up block a
+    // shard) when Fs % 32 == 0
+    p.flat_n = (!h->swiglu || Fs % 32 == 0) ? 1 : 0;
     p.tiles_per_shard = static_cast<int>(cdiv(Fs, kBN));
-    p.num_n_tiles = static_cast<int>(t * p.tiles_per_shard);
+    p.num_n_tiles = static_cast<int>(p.flat_n ? cdiv(F, kBN) : t * p.tiles_per_shard);
     p.num_kb = static_cast<int>(cdiv(H, kBK));
     p.aux = static_cast<const __nv_bfloat16*>(Zsaved);
     p.out0 = dZ;

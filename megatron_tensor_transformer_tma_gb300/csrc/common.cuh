@@ -77,29 +77,6 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
                : "memory");
 }
 
-// 32-byte store of eight 32-bit words (one full 32-byte sector; the address must be
-// 32-byte aligned).  kEvictFirst marks the line as the first to leave L2.
-template <bool kEvictFirst = false>
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
-  if constexpr (kEvictFirst)
-    asm volatile("st.global.L2::evict_first.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
-                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                 "r"(w[7])
-                 : "memory");
-  else
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
-                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-// Read-only 32-byte load (ld.global.nc.v8; 32-byte aligned address).
-__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t (&w)[8]) {
-  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
-        "=r"(w[7])
-      : "l"(p));
-}
-
 // Read-only 16-byte load (ld.global.nc).  Not an asm volatile: the compiler must be free
 // to hoist a batch of these ahead of their uses so that they are in flight together.
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {

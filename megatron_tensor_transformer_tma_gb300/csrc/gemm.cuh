@@ -52,19 +52,6 @@
 #include "fp8.cuh"
 #include "gemm_params.h"
 
-#ifndef MLPB_DGRAD_V8
-#define MLPB_DGRAD_V8 0
-#endif
-#ifndef MLPB_FC1_V8
-#define MLPB_FC1_V8 0
-#endif
-#ifndef MLPB_F32_V8
-#define MLPB_F32_V8 0
-#endif
-#ifndef MLPB_EPI_SLEEP
-#define MLPB_EPI_SLEEP 0
-#endif
-
 namespace mlpb {
 
 template <GemmKind K>
@@ -167,52 +154,7 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, cons
   }
 }
 
-// The same with 32-byte accesses: two per 32 values, whole sectors (p 32-byte aligned and
-// nvalid a multiple of 16).
-__device__ __forceinline__ void load_bf16x32_v8(const __nv_bfloat16* p, int nvalid,
-                                                float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (q * 16 < nvalid) ld_global_nc_v8(p + q * 16, w);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 f = unpack_bf16x2(w[e]);
-      v[q * 16 + 2 * e] = f.x;
-      v[q * 16 + 2 * e + 1] = f.y;
-    }
-  }
-}
-
-template <bool kEvictFirst = false>
-__device__ __forceinline__ void store_bf16x32_v8(__nv_bfloat16* p, int nvalid,
-                                                 const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    if (q * 16 < nvalid) {
-      uint32_t w[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[q * 16 + 2 * e], v[q * 16 + 2 * e + 1]);
-      st_global_v8<kEvictFirst>(p + q * 16, w);
-    }
-  }
-}
-
 __device__ __forceinline__ void store_f32x32(float* p, int nvalid, const float (&v)[32]) {
-#if MLPB_F32_V8
-  if ((nvalid & 7) == 0) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (q * 8 < nvalid) {
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[q * 8 + e]);
-        st_global_v8(p + q * 8, w);
-      }
-    }
-    return;
-  }
-#endif
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     if (q * 4 < nvalid) {
@@ -306,19 +248,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] += b[e];
       }
-#if MLPB_FC1_V8
-      if (row_ok) store_bf16x32_v8(Z + col, nv, v);
-#else
       if (row_ok) store_bf16x32(Z + col, nv, v);
-#endif
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
       if (row_ok) {
-#if MLPB_FC1_V8
-        store_bf16x32_v8(A + col, nv, v);
-#else
         store_bf16x32(A + col, nv, v);
-#endif
         if constexpr (F8) track_amax(v, nv, am);
       }
     }
@@ -377,91 +311,74 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
           store_f32x32(static_cast<float*>(p.out0) + yo + col, nv, v);
       }
     }
-  } else if constexpr (K == GemmKind::DGRAD_GELU) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
-    const size_t base = static_cast<size_t>(m) * p.F + static_cast<size_t>(i) * p.Fs;
-    const __nv_bfloat16* Z = p.aux + base;
-    __nv_bfloat16* dZ = static_cast<__nv_bfloat16*>(p.out0) + base;
-    // recomputation: A = gelu(Z) from the saved Z, for the dW2 GEMM that follows
-    __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + base : nullptr;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int jc = j0 + c * 32;
-      if (jc >= p.Fs) break;
-      float v[32], z[32];
-      load_acc<F8>(tacc + c * 32, v, sc);
-      const int nv = min(32, p.Fs - jc);
-      if (row_ok) {
-#if MLPB_DGRAD_V8 & 2
-        load_bf16x32_v8(Z + jc, nv, z);
-#else
-        load_bf16x32(Z + jc, nv, z);
-#endif
-        if (A != nullptr) {
-          float a[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = gelu_f(z[e]);
-          store_bf16x32(A + jc, nv, a);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
-#if MLPB_DGRAD_V8 & 1
-        store_bf16x32_v8<(MLPB_DGRAD_V8 & 4) != 0>(dZ + jc, nv, v);
-#else
-        store_bf16x32(dZ + jc, nv, v);
-#endif
-        if constexpr (F8) track_amax(v, nv, am);
-      }
-      if (p.colsum != nullptr) {  // db1 partials: column sums of the stored (bf16) dZ
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          v[e] = row_ok ? __bfloat162float(__float2bfloat16_rn(v[e])) : 0.0f;
-        const float cs = warp_column_sums(v);
-        const int lane = threadIdx.x & 31;
-        if (lane < nv)
-          p.colsum[static_cast<size_t>(m >> 5) * p.F + static_cast<size_t>(i) * p.Fs + jc + lane] = cs;
-      }
-#if MLPB_EPI_SLEEP
-      __nanosleep(MLPB_EPI_SLEEP);
-#endif
+  } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
+    // The tile's dA columns f0.. (global indices into F) end at f_end: all of F when the N
+    // tiles run across shard seams, else shard i's end.
+    int f0 = nt * kBN, f_end = p.F;
+    if (!p.flat_n) {
+      const int i = nt / p.tiles_per_shard;
+      f0 = i * p.Fs + (nt - i * p.tiles_per_shard) * kBN;
+      f_end = (i + 1) * p.Fs;
     }
-  } else if constexpr (K == GemmKind::DGRAD_SWIGLU) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN;
-    const size_t base = static_cast<size_t>(m) * 2 * p.F + static_cast<size_t>(i) * 2 * p.Fs;
-    const __nv_bfloat16* GU = p.aux + base;
-    __nv_bfloat16* dGU = static_cast<__nv_bfloat16*>(p.out0) + base;
-    // recomputation: A = silu(G) U from the saved G, U, for the dW2 GEMM that follows
-    __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F +
-                                    static_cast<size_t>(i) * p.Fs
+    // recomputation: A [T][F] rewritten from the saved Z (or G, U), for the dW2 GEMM that
+    // follows
+    __nv_bfloat16* A = p.out1 ? static_cast<__nv_bfloat16*>(p.out1) + static_cast<size_t>(m) * p.F
                               : nullptr;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
-      const int jc = j0 + c * 32;
-      if (jc >= p.Fs) break;
-      float da[32];
-      load_acc<F8>(tacc + c * 32, da, sc);
-      const int nv = min(32, p.Fs - jc);
-      if (row_ok) {
+      const int f = f0 + c * 32;
+      if (f >= f_end) break;
+      const int nv = min(32, f_end - f);
+      float v[32];
+      load_acc<F8>(tacc + c * 32, v, sc);
+      if constexpr (K == GemmKind::DGRAD_GELU) {
+        const size_t o = static_cast<size_t>(m) * p.F + f;  // Z, dZ [T][F]
+        if (row_ok) {
+          float z[32];
+          load_bf16x32(p.aux + o, nv, z);
+          if (A != nullptr) {
+            float a[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = gelu_f(z[e]);
+            store_bf16x32(A + f, nv, a);
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, nv, v);
+          if constexpr (F8) track_amax(v, nv, am);
+        }
+        if (p.colsum != nullptr) {  // db1 partials: column sums of the stored (bf16) dZ
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[e] = row_ok ? __bfloat162float(__float2bfloat16_rn(v[e])) : 0.0f;
+          const float cs = warp_column_sums(v);
+          const int lane = threadIdx.x & 31;
+          if (lane < nv) p.colsum[static_cast<size_t>(m >> 5) * p.F + f + lane] = cs;
+        }
+      } else if (row_ok) {
+        // G|U, dG|dU [T][2F]: shard i's Fs gate columns, then its Fs up columns (the
+        // chunk lies in one shard: Fs % 32 == 0 when tiles cross seams)
+        const int i = f / p.Fs;
+        const size_t o = static_cast<size_t>(m) * 2 * p.F + f + static_cast<size_t>(i) * p.Fs;
         float g[32], u[32];
-        load_bf16x32(GU + jc, nv, g);
-        load_bf16x32(GU + p.Fs + jc, nv, u);
+        load_bf16x32(p.aux + o, nv, g);
+        load_bf16x32(p.aux + o + p.Fs, nv, u);
         if (A != nullptr) {
           float a[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = u[e] * (g[e] * sigmoid_f(g[e]));
-          store_bf16x32(A + jc, nv, a);
+          store_bf16x32(A + f, nv, a);
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float s = sigmoid_f(g[e]);
-          const float dg = da[e] * u[e] * s * (1.0f + g[e] * (1.0f - s));
-          u[e] = da[e] * g[e] * s;  // dU
-          g[e] = dg;                // dG
+          const float dg = v[e] * u[e] * s * (1.0f + g[e] * (1.0f - s));
+          u[e] = v[e] * g[e] * s;  // dU
+          g[e] = dg;               // dG
         }
-        store_bf16x32(dGU + jc, nv, g);
-        store_bf16x32(dGU + p.Fs + jc, nv, u);
+        __nv_bfloat16* dGU = static_cast<__nv_bfloat16*>(p.out0) + o;
+        store_bf16x32(dGU, nv, g);
+        store_bf16x32(dGU + p.Fs, nv, u);
         if constexpr (F8) {
           track_amax(g, nv, am);
           track_amax(u, nv, am);
@@ -611,11 +528,15 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
     ld2<kPeer>(sa, tA, bar, i * p.Fs + j0, mt * kBM);
     ld2<kPeer>(sb, tB, bar, j0, i * p.H + nh);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
-    // B = W2's transposed copy [F][H]: shard i's rows j0.. (K-major)
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
+    // B = W2's transposed copy [F][H] (K-major): rows nh.. over all of F, or shard i's
+    // rows j0..
+    int row = nh;
+    if (!p.flat_n) {
+      const int i = nt / p.tiles_per_shard;
+      row = i * p.Fs + (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
+    }
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
-    ld2<kPeer>(sb, tB, bar, k0, i * p.Fs + j0);
+    ld2<kPeer>(sb, tB, bar, k0, row);
   } else if constexpr (K == GemmKind::DX) {
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
 #pragma unroll

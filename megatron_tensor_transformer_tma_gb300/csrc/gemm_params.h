@@ -66,6 +66,11 @@ struct GemmParams {
   // DGRAD_GELU with a bias: each warp writes the column sums of its 32 rows of the bf16 dZ
   // it stores, colsum[m / 32][f] ([T/32][F] fp32), for the db1 reduction; NULL: none.
   float* colsum;
+  // DGRAD_* (bf16): N tiles run over all F columns of dA, across shard seams (B is W2's
+  // transposed copy [F][H], one K-major matrix), so no shard pads its last tile; the
+  // SwiGLU epilogue needs Fs % 32 == 0 for this (a 32-column chunk in one shard).  0: N
+  // tiles of 256 within each shard (tiles_per_shard a shard).
+  int flat_n;
 };
 
 // FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.
