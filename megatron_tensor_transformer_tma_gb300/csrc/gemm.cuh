@@ -140,6 +140,20 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid,
   }
 }
 
+// 32 values rounded to bf16 (nearest, ties to even), two to a word: w[e] = (v[2e], v[2e+1]).
+__device__ __forceinline__ void pack_bf16x32(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+}
+
+__device__ __forceinline__ void store_packed_bf16x32(__nv_bfloat16* p, int nvalid,
+                                                     const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q * 8 < nvalid)
+      st_global_v4(p + q * 8, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+}
+
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -333,6 +347,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       load_acc<F8>(tacc + c * 32, v, sc);
       if constexpr (K == GemmKind::DGRAD_GELU) {
         const size_t o = static_cast<size_t>(m) * p.F + f;  // Z, dZ [T][F]
+        uint32_t w[16];  // the stored bf16 dZ, two to a word
         if (row_ok) {
           float z[32];
           load_bf16x32(p.aux + o, nv, z);
@@ -344,13 +359,19 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, nv, v);
+          pack_bf16x32(v, w);
+          store_packed_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, nv, w);
           if constexpr (F8) track_amax(v, nv, am);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
         }
         if (p.colsum != nullptr) {  // db1 partials: column sums of the stored (bf16) dZ
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = row_ok ? __bfloat162float(__float2bfloat16_rn(v[e])) : 0.0f;
+          for (int e = 0; e < 16; ++e) {  // a bf16 is the high half of the float it equals
+            v[2 * e] = __uint_as_float(w[e] << 16);
+            v[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
           const float cs = warp_column_sums(v);
           const int lane = threadIdx.x & 31;
           if (lane < nv) p.colsum[static_cast<size_t>(m >> 5) * p.F + f + lane] = cs;
