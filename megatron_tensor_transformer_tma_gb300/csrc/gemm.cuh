@@ -489,6 +489,33 @@ __device__ __forceinline__ void ld4(uint32_t d, const CUtensorMap* m, uint32_t b
   else tma_load_4d(d, m, bar, c0, c1, c2, c3);
 }
 
+// The k-block a stage loads and, for FC2 (whose K loop walks the shards), its shard and
+// its k-block within the shard.  The producer steps it with kb, so no stage divides.
+struct KPos {
+  int kb, sh, kr;
+};
+
+template <GemmKind K>
+__device__ __forceinline__ void step_kpos(KPos& kp, bool rev, const GemmParams& p) {
+  if (rev) {
+    --kp.kb;
+    if constexpr (K == GemmKind::FC2) {
+      if (--kp.kr < 0) {
+        kp.kr = p.kb_per_shard - 1;
+        --kp.sh;
+      }
+    }
+  } else {
+    ++kp.kb;
+    if constexpr (K == GemmKind::FC2) {
+      if (++kp.kr == p.kb_per_shard) {
+        kp.kr = 0;
+        ++kp.sh;
+      }
+    }
+  }
+}
+
 // One stage of one CTA of the pair: its own 128 A rows, and its 128-row half of B (K-major:
 // one box; MN-major: two 64-wide chunks).
 // FP8: every operand is K-major (E4M3 copies, transposed where needed), one box each:
@@ -501,8 +528,9 @@ __device__ __forceinline__ void ld4(uint32_t d, const CUtensorMap* m, uint32_t b
 template <GemmKind K, bool kPeer>
 __device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUtensorMap* tB,
                                                uint32_t sa, uint32_t sb, uint32_t bar, int mt,
-                                               int nt, int kb, int rank, const GemmParams& p) {
-  const int k0 = kb * kBK8;
+                                               int nt, const KPos& kp, int rank,
+                                               const GemmParams& p) {
+  const int k0 = kp.kb * kBK8;
   const int nh = nt * kBN + 128 * rank;
   if constexpr (K == GemmKind::FC1_GELU || K == GemmKind::DX || K == GemmKind::WGRAD_W1) {
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
@@ -513,10 +541,9 @@ __device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUte
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
     ld4<kPeer>(sb, tB, bar, k0, j0, rank, i);
   } else if constexpr (K == GemmKind::FC2) {
-    const int i = kb / p.kb_per_shard;
-    const int j0 = (kb - i * p.kb_per_shard) * kBK8;
-    ld3<kPeer>(sa, tA, bar, j0, mt * kBM, i);
-    ld3<kPeer>(sb, tB, bar, j0, nh, i);
+    const int j0 = kp.kr * kBK8;
+    ld3<kPeer>(sa, tA, bar, j0, mt * kBM, kp.sh);
+    ld3<kPeer>(sb, tB, bar, j0, nh, kp.sh);
   } else {  // DGRAD_*, WGRAD_W2: B rows are shard i's rows j0.. of a [t][Fs][K] operand
     const int i = nt / p.tiles_per_shard;
     const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
@@ -528,8 +555,9 @@ __device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUte
 template <GemmKind K, bool kPeer>
 __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CUtensorMap* tB,
                                                  uint32_t sa, uint32_t sb, uint32_t bar, int mt,
-                                                 int nt, int kb, int rank,
+                                                 int nt, const KPos& kp, int rank,
                                                  const GemmParams& p) {
+  const int kb = kp.kb;
   static_assert(K != GemmKind::WGRAD_W2, "the bf16 dW2 is the transposed WGRAD_W2T");
   const int k0 = kb * kBK;
   const int nh = nt * kBN + 128 * rank;  // first B row (N index) of this CTA's half
@@ -544,8 +572,8 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
     ld2<kPeer>(sb, tB, bar, k0, (2 * i + rank) * p.Fs + j0);
   } else if constexpr (K == GemmKind::FC2) {
     // K walks the shards: A [T][F] at shard i's columns, W2 as [tH][Fs] at shard i's rows
-    const int i = kb / p.kb_per_shard;
-    const int j0 = (kb - i * p.kb_per_shard) * kBK;
+    const int i = kp.sh;
+    const int j0 = kp.kr * kBK;
     ld2<kPeer>(sa, tA, bar, i * p.Fs + j0, mt * kBM);
     ld2<kPeer>(sb, tB, bar, j0, i * p.H + nh);
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
@@ -649,9 +677,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // tile shares an operand panel with this one (the grouped raster), and it starts
         // on the k-blocks just read, which are still in L2 (5-10 % less DRAM traffic)
         const bool rev = KindOf<K>::reverse_k && part < 0 && (it & 1) != 0;
+        KPos kp{rev ? kb1 - 1 : kb0, 0, 0};
+        if constexpr (K == GemmKind::FC2) {  // one division a tile; then stepped
+          kp.sh = kp.kb / p.kb_per_shard;
+          kp.kr = kp.kb - kp.sh * p.kb_per_shard;
+        }
         bool ok = true;
         for (int i = kb0; i < kb1; ++i) {
-          const int kb = rev ? kb0 + kb1 - 1 - i : i;
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -665,19 +697,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, 2 * kPairStageBytes);
             if constexpr (F8)
-              issue_stage_f8<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+              issue_stage_f8<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kp, rank, p);
             else
-              issue_stage_pair<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+              issue_stage_pair<K, false>(&tmA, &tmB, sa, sb, fb, mt, nt, kp, rank, p);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           } else {
             const uint32_t fb = full_lead + 8 * stage;
             if constexpr (F8)
-              issue_stage_f8<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+              issue_stage_f8<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kp, rank, p);
             else
-              issue_stage_pair<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kb, rank, p);
+              issue_stage_pair<K, true>(&tmA, &tmB, sa, sb, fb, mt, nt, kp, rank, p);
             armed = 1u;  // issued copies that nothing in this CTA observes
           }
+          step_kpos<K>(kp, rev, p);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
