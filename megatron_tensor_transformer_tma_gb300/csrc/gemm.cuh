@@ -490,9 +490,12 @@ __device__ __forceinline__ void ld4(uint32_t d, const CUtensorMap* m, uint32_t b
 }
 
 // The k-block a stage loads and, for FC2 (whose K loop walks the shards), its shard and
-// its k-block within the shard.  The producer steps it with kb, so no stage divides.
+// its k-block within the shard; for the kinds whose N tiles lie in one shard, the tile's
+// shard ts and its tile index tj within the shard.  The producer sets ts, tj once a tile
+// and steps the rest with kb, so no stage divides.
 struct KPos {
   int kb, sh, kr;
+  int ts, tj;
 };
 
 template <GemmKind K>
@@ -536,19 +539,15 @@ __device__ __forceinline__ void issue_stage_f8(const CUtensorMap* tA, const CUte
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
     ld2<kPeer>(sb, tB, bar, k0, nh);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * 128;
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
-    ld4<kPeer>(sb, tB, bar, k0, j0, rank, i);
+    ld4<kPeer>(sb, tB, bar, k0, kp.tj * 128, rank, kp.ts);
   } else if constexpr (K == GemmKind::FC2) {
     const int j0 = kp.kr * kBK8;
     ld3<kPeer>(sa, tA, bar, j0, mt * kBM, kp.sh);
     ld3<kPeer>(sb, tB, bar, j0, nh, kp.sh);
   } else {  // DGRAD_*, WGRAD_W2: B rows are shard i's rows j0.. of a [t][Fs][K] operand
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
-    ld3<kPeer>(sb, tB, bar, k0, j0, i);
+    ld3<kPeer>(sb, tB, bar, k0, kp.tj * kBN + 128 * rank, kp.ts);
   }
 }
 
@@ -566,10 +565,8 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
     ld2<kPeer>(sb, tB, bar, k0, nh);
   } else if constexpr (K == GemmKind::FC1_SWIGLU) {
     // W1 as [2F][H]: shard i's gate rows (even CTA) or up rows (odd CTA) j0..
-    const int i = nt / p.tiles_per_shard;
-    const int j0 = (nt - i * p.tiles_per_shard) * 128;
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
-    ld2<kPeer>(sb, tB, bar, k0, (2 * i + rank) * p.Fs + j0);
+    ld2<kPeer>(sb, tB, bar, k0, (2 * kp.ts + rank) * p.Fs + kp.tj * 128);
   } else if constexpr (K == GemmKind::FC2) {
     // K walks the shards: A [T][F] at shard i's columns, W2 as [tH][Fs] at shard i's rows
     const int i = kp.sh;
@@ -579,11 +576,7 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
   } else if constexpr (K == GemmKind::DGRAD_GELU || K == GemmKind::DGRAD_SWIGLU) {
     // B = W2's transposed copy [F][H] (K-major): rows nh.. over all of F, or shard i's
     // rows j0..
-    int row = nh;
-    if (!p.flat_n) {
-      const int i = nt / p.tiles_per_shard;
-      row = i * p.Fs + (nt - i * p.tiles_per_shard) * kBN + 128 * rank;
-    }
+    const int row = p.flat_n ? nh : kp.ts * p.Fs + kp.tj * kBN + 128 * rank;
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
     ld2<kPeer>(sb, tB, bar, k0, row);
   } else if constexpr (K == GemmKind::DX) {
@@ -677,10 +670,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // tile shares an operand panel with this one (the grouped raster), and it starts
         // on the k-blocks just read, which are still in L2 (5-10 % less DRAM traffic)
         const bool rev = KindOf<K>::reverse_k && part < 0 && (it & 1) != 0;
-        KPos kp{rev ? kb1 - 1 : kb0, 0, 0};
+        KPos kp{rev ? kb1 - 1 : kb0, 0, 0, 0, 0};
         if constexpr (K == GemmKind::FC2) {  // one division a tile; then stepped
           kp.sh = kp.kb / p.kb_per_shard;
           kp.kr = kp.kb - kp.sh * p.kb_per_shard;
+        }
+        if constexpr (K == GemmKind::FC1_SWIGLU || K == GemmKind::DGRAD_GELU ||
+                      K == GemmKind::DGRAD_SWIGLU || K == GemmKind::WGRAD_W2) {
+          kp.ts = nt / p.tiles_per_shard;
+          kp.tj = nt - kp.ts * p.tiles_per_shard;
         }
         bool ok = true;
         for (int i = kb0; i < kb1; ++i) {
@@ -741,6 +739,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr bool b_mn = !F8 && KindOf<K>::b_mn;
       constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(2 * kBM, kBN)
                                     : idesc_bf16_f32(2 * kBM, kBN, a_mn, b_mn);
+      // Shared-memory descriptors of stage 0; a stage's and an MMA's are these plus an
+      // offset in the 14-bit address field (byte address / 16), which cannot carry out of
+      // the field: shared memory ends below 256 KB.
+      static_assert(kPairSmem < 256 * 1024, "descriptor address field");
+      const uint64_t adesc0 = a_mn ? sdesc(sA0, kChunk, 1024, 2u) : sdesc(sA0, 16, 1024, 2u);
+      const uint64_t bdesc0 = b_mn ? sdesc(sB0, kChunk, 1024, 2u) : sdesc(sB0, 16, 1024, 2u);
+      constexpr uint32_t kAk = (a_mn ? 2048u : 32u) >> 4, kBk = (b_mn ? 2048u : 32u) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -759,15 +764,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sA0 + stage * kPairAStage;
-          const uint32_t sb = sB0 + stage * kPairBStage;
+          const uint64_t as = adesc0 + static_cast<uint32_t>(stage) * (kPairAStage >> 4);
+          const uint64_t bs = bdesc0 + static_cast<uint32_t>(stage) * (kPairBStage >> 4);
           // four MMAs a stage: K = 16 bf16 or 32 E4M3 each, 32 bytes of every K-major row
+          // (MN-major: the next 8-row group of K, 2 KB on)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = a_mn ? sdesc(sa + kk * 2048, kChunk, 1024, 2u)
-                                     : sdesc(sa + kk * 32, 16, 1024, 2u);
-            const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, kChunk, 1024, 2u)
-                                     : sdesc(sb + kk * 32, 16, 1024, 2u);
+            const uint64_t ad = as + kk * kAk;
+            const uint64_t bd = bs + kk * kBk;
             const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
             if constexpr (F8)
               umma_f8_pair(d, ad, bd, idesc, accumulate);
