@@ -65,10 +65,12 @@ struct KindOf {
                                 K == GemmKind::WGRAD_W2T);
 };
 
-// Grouped rasterisation: 8 consecutive M tiles (or M-tile pairs) sweep all N tiles
-// together so that the B tiles they share stay in L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mt, int& nt) {
-  constexpr int G = 8;
+// Grouped rasterisation: `group` consecutive M tiles (or M-tile pairs; 0: 8) sweep all N
+// tiles together, so that the B panels they share stay in L2 while the group's A panels
+// are read once.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int& mt,
+                                            int& nt) {
+  const int G = group > 0 ? group : 8;
   const int span = G * num_n;
   const int g = tile / span;
   const int m0 = g * G;
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int st, kb0, kb1, part;
         unit_range(u, split, split_start, p.num_kb, st, kb0, kb1, part);
         int mp, nt;
-        tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
+        tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, mp, nt);
         const int mt = mp * 2 + rank;
         // long-K GEMMs: whole tiles of odd iterations walk K backwards.  The pair's next
         // tile shares an operand panel with this one (the grouped raster), and it starts
@@ -810,7 +812,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       tc_fence_after();
       int mp, nt;
-      tile_coords(st, num_pm, p.num_n_tiles, mp, nt);
+      tile_coords(st, num_pm, p.num_n_tiles, p.raster_group, mp, nt);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kBN;
       float am = 0.0f;
       if (part >= 0) {  // a K-range of a tail tile: raw partial sums, summed by the fixup

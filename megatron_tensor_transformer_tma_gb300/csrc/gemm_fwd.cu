@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const GemmParams p) {
   const int c = (threadIdx.x & 31) * 8;
   const int num_pm = (p.num_m_tiles + 1) / 2;
   int mp, nt;
-  tile_coords(p.split_start + j, num_pm, p.num_n_tiles, mp, nt);
+  tile_coords(p.split_start + j, num_pm, p.num_n_tiles, p.raster_group, mp, nt);
   const int m = (mp * 2 + rank) * kBM + r;
   const int n = nt * kBN + c;
   if (m >= p.M || n >= p.H) return;

@@ -71,6 +71,8 @@ struct GemmParams {
   // SwiGLU epilogue needs Fs % 32 == 0 for this (a 32-column chunk in one shard).  0: N
   // tiles of 256 within each shard (tiles_per_shard a shard).
   int flat_n;
+  // M-tile pairs in a raster group (tile_coords); 0: 8.
+  int raster_group;
 };
 
 // FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.
