@@ -104,6 +104,19 @@ bool map2d(CUtensorMap* m, const void* p, uint64_t inner, uint64_t outer, uint64
   return encode_bf16(m, p, 2, dims, str, box);
 }
 
+// An MN-major operand [rows][mn] (rows along K) as a 3-D map {64, rows, mn / 64} whose
+// third dimension steps 64 columns (128 bytes): one box {64, 64, 2} brings both 64-column
+// chunks of a CTA's 128-wide half, chunk after chunk, the order the MMA's MN-major
+// descriptors read -- one copy a stage instead of two.  Needs mn % 64 == 0 (a chunk past
+// the end then reads zeros, not the next row); false when it cannot be built.
+bool map_mn3d(CUtensorMap* m, const void* p, uint64_t mn, uint64_t rows, uint64_t ld_elems) {
+  if (mn % 64 != 0) return false;
+  const uint64_t dims[3] = {64, rows, mn / 64};
+  const uint64_t str[2] = {ld_elems * 2, 128};
+  const uint32_t box[3] = {64, 64, 2};
+  return encode_bf16(m, p, 3, dims, str, box);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -793,15 +806,24 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
 
   // Tensor maps of all four GEMMs first: an encoding error launches nothing.
   CUtensorMap tdgA, tdgB, tw2A, tw2B, tw1A, tw1B, tdxA, tdxB;
+  int mn3d_w2 = 0, mn3d_w1 = 0, mn3d_dx = 0;
   void* w2t = ws + ws_w2t_offset(h);
   {
     // the dgrad's B is W2's per-shard transpose [F][H] (K-major rows i Fs + j), written by
     // the transpose below; with N tiles per shard, a 128-row box past shard i's Fs rows
     // reads the next shard's rows, which land in output columns the epilogue drops
     if (!map2d(&tdgA, dY, H, T, H, kBK, kBM) || !map2d(&tdgB, w2t, H, F, H, kBK, kBN / 2) ||
-        !map2d(&tw2A, Asaved, F, T, F, 64, kBK) || !map2d(&tw2B, dY, H, T, H, 64, kBK) ||
-        !map2d(&tw1A, dZ, F1, T, F1, 64, kBK) || !map2d(&tw1B, X, H, T, H, 64, kBK) ||
-        !map2d(&tdxA, dZ, F1, T, F1, kBK, kBM) || !map2d(&tdxB, W1, H, F1, H, 64, kBK))
+        !map2d(&tdxA, dZ, F1, T, F1, kBK, kBM))
+      return MLPB_EINVAL;
+    // the MN-major operands: 3-D maps (one copy a stage) where they can be built
+    mn3d_w2 = (map_mn3d(&tw2A, Asaved, F, T, F) ? 1 : 0) | (map_mn3d(&tw2B, dY, H, T, H) ? 2 : 0);
+    mn3d_w1 = (map_mn3d(&tw1A, dZ, F1, T, F1) ? 1 : 0) | (map_mn3d(&tw1B, X, H, T, H) ? 2 : 0);
+    mn3d_dx = map_mn3d(&tdxB, W1, H, F1, H) ? 2 : 0;
+    if ((!(mn3d_w2 & 1) && !map2d(&tw2A, Asaved, F, T, F, 64, kBK)) ||
+        (!(mn3d_w2 & 2) && !map2d(&tw2B, dY, H, T, H, 64, kBK)) ||
+        (!(mn3d_w1 & 1) && !map2d(&tw1A, dZ, F1, T, F1, 64, kBK)) ||
+        (!(mn3d_w1 & 2) && !map2d(&tw1B, X, H, T, H, 64, kBK)) ||
+        (!(mn3d_dx & 2) && !map2d(&tdxB, W1, H, F1, H, 64, kBK)))
       return MLPB_EINVAL;
   }
 
@@ -868,6 +890,7 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW2;
     p.accumulate = acc;
+    p.mn3d = mn3d_w2;
     st = run_gemm(h, GemmKind::WGRAD_W2T, false, tw2A, tw2B, p, s2, "wgrad_w2", 2.0 * H * F * T,
                   2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
@@ -890,6 +913,7 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
     p.num_kb = static_cast<int>(T / kBK);
     p.out0 = dW1;
     p.accumulate = acc;
+    p.mn3d = mn3d_w1;
     plan_tail_split(h, p, ws_split_partial(h, workspace, 1));  // the last GEMM of the step
     st = run_gemm(h, GemmKind::WGRAD_W1, false, tw1A, tw1B, p, s2, "wgrad_w1", 2.0 * F1 * H * T,
                   2.0 * (T * F1 + T * H) + 4.0 * (1 + acc) * F1 * H);
@@ -904,6 +928,7 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
     p.num_kb = static_cast<int>(cdiv(F1, kBK));
     p.out0 = dX;
     p.out_bf16 = h->bf16_out ? 1 : 0;
+    p.mn3d = mn3d_dx;
     plan_tail_split(h, p, ws_split_partial(h, workspace));
     st = run_gemm(h, GemmKind::DX, false, tdxA, tdxB, p, s, "dgrad_x", 2.0 * T * H * F1,
                   2.0 * (T * F1 + F1 * H) + (h->bf16_out ? 2.0 : 4.0) * T * H);

@@ -583,13 +583,25 @@ __device__ __forceinline__ void issue_stage_pair(const CUtensorMap* tA, const CU
     ld2<kPeer>(sb, tB, bar, k0, row);
   } else if constexpr (K == GemmKind::DX) {
     ld2<kPeer>(sa, tA, bar, k0, mt * kBM);
+    if (p.mn3d & 2) {
+      ld3<kPeer>(sb, tB, bar, 0, k0, nh >> 6);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+      for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+    }
   } else {  // WGRAD_W1, WGRAD_W2T
+    if (p.mn3d & 1) {
+      ld3<kPeer>(sa, tA, bar, 0, k0, (mt * kBM) >> 6);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) ld2<kPeer>(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+      for (int q = 0; q < 2; ++q) ld2<kPeer>(sa + q * kChunk, tA, bar, mt * kBM + 64 * q, k0);
+    }
+    if (p.mn3d & 2) {
+      ld3<kPeer>(sb, tB, bar, 0, k0, nh >> 6);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+      for (int q = 0; q < 2; ++q) ld2<kPeer>(sb + q * kChunk, tB, bar, nh + 64 * q, k0);
+    }
   }
 }
 

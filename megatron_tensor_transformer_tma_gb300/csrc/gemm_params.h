@@ -73,6 +73,9 @@ struct GemmParams {
   int flat_n;
   // M-tile pairs in a raster group (tile_coords); 0: 8.
   int raster_group;
+  // MN-major operands loaded through a 3-D map, one box of both 64-wide chunks a stage:
+  // bit 0 A, bit 1 B (else two 2-D boxes).
+  int mn3d;
 };
 
 // FP8 stage: the same 16 KB A and B-half tiles, 128 one-byte elements deep.
