@@ -169,10 +169,11 @@ void mlpb_destroy(mlpb_handle *h);
 
 /* Bytes of device scratch the caller passes as `workspace` to mlpb_forward,
  * mlpb_backward and mlpb_layernorm_sp_bwd (it holds dZ [T][F1] bf16, with a bias the
- * db1 column sums of each 32-row group of dZ that the dgrad epilogue writes, a transposed
- * copy of W2 ([F][H] bf16, the dgrad GEMM's operand; not under MLPB_FLAG_FP8), two regions of fp32 partial tiles for the K-range split of a GEMM's last
- * wave -- dX and dW1 run at once on two streams -- and, under MLPB_FLAG_FP8, the
- * E4M3 operand copies and their amax words). */
+ * db1 column sums of each 32-row group of dZ that the dgrad epilogue writes, two regions
+ * of fp32 partial tiles for the K-range split of a GEMM's last wave -- dX and dW1 run at
+ * once on two streams -- a transposed copy of W2 ([F][H] bf16, the dgrad GEMM's operand)
+ * (not under MLPB_FLAG_FP8), with a bias db2's column sums over row ranges of dY, and,
+ * under MLPB_FLAG_FP8, the E4M3 operand copies and their amax words). */
 mlpb_status mlpb_workspace_size(const mlpb_handle *h, size_t *bytes);
 
 /* Bytes of the saved activations: z_bytes for Z (GELU, T*F*2) or G|U (SwiGLU,
@@ -195,7 +196,9 @@ mlpb_status mlpb_forward(mlpb_handle *h, const void *X, const void *W1, const vo
 /* Backward of the block for an upstream gradient dY [T][H] bf16.  g backward is
  * the identity (every shard reads the same dY); dZ = (dY W2_i) * act'(.) per
  * shard; dW2_i = dY^T A_i; dW1_i = dZ_i^T X; db1 = sum_t dZ (column sums of the bf16
- * dZ taken in the dgrad epilogue, then added in row order); db2 = sum_t dY (one launch);
+ * dZ taken in the dgrad epilogue, then added in row order); db2 = sum_t dY (column sums
+ * over row ranges taken in the launch that transposes W2 -- under MLPB_FLAG_FP8 in one of
+ * its own -- then added in row-range order);
  * dX = sum_i dZ_i W1_i with the sum over shards accumulated in one tensor-memory
  * accumulator (the emulated f all-reduce).  db1/db2 must be NULL without bias.
  * `workspace` must hold mlpb_workspace_size() bytes.  Asaved is read only (the

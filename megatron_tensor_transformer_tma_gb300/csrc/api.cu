@@ -317,7 +317,20 @@ size_t ws_w2t_bytes(const mlpb_handle* h) {
   return h->fp8 ? 0 : align256(static_cast<size_t>(h->F * h->H * 2));
 }
 
-size_t ws_backward_bytes(const mlpb_handle* h) { return ws_w2t_offset(h) + ws_w2t_bytes(h); }
+// Row ranges of db2's first pass (written beside the W2 transpose): 256 rows each, at most
+// 64, so that the column-sum blocks (H / 256 per range) spread over the GPU.
+int db2_splits(const mlpb_handle* h) {
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, h->T / 256)));
+}
+
+// db2's partial rows [splits][H] fp32 (with a bias), after W2's copy.
+size_t ws_db2_offset(const mlpb_handle* h) { return ws_w2t_offset(h) + ws_w2t_bytes(h); }
+
+size_t ws_db2_bytes(const mlpb_handle* h) {
+  return h->cfg.has_bias ? align256(static_cast<size_t>(db2_splits(h)) * h->H * 4) : 0;
+}
+
+size_t ws_backward_bytes(const mlpb_handle* h) { return ws_db2_offset(h) + ws_db2_bytes(h); }
 
 float* ws_split_partial(const mlpb_handle* h, void* workspace, int region = 0) {
   return workspace == nullptr
@@ -831,23 +844,20 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
   // CUDA-event interval is its own and not shared with a concurrent one.
   cudaStream_t s2 = h->timing ? s : h->side;
 
-  // Fork: stream s2 starts with db2, which needs only dY; after dgrad it runs dW2, db1, dW1.
+  // Fork: after dgrad, stream s2 runs dW2, the bias sums and dW1 beside dX.
   if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
       cudaStreamWaitEvent(s2, h->ev_fork, 0) != cudaSuccess)
     return MLPB_ECUDA;
 
-  // ---- [s2] db2 = sum_t dY  (g backward is the identity: the bias sees dY itself)
-  if (bias) {
-    LaunchTimer lt(h, s2, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
-    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, h->num_sms, s2, acc);
-    lt.done();
-    st = from_cuda(e);
-  }
-
-  // ---- [s] W2's per-shard transpose for the dgrad (K-major B), beside db2
-  if (st == MLPB_OK) {
-    LaunchTimer lt(h, s, "w2_transpose", 0.0, 4.0 * F * H);
-    cudaError_t e = launch_transpose_w2(W2, w2t, static_cast<int>(t), H, Fs, s);
+  // ---- [s] W2's per-shard transpose for the dgrad (K-major B) and, in the same launch,
+  // the first pass of db2 = sum_t dY (g backward is the identity: the bias sees dY itself)
+  float* part2 = reinterpret_cast<float*>(ws + ws_db2_offset(h));  // db2 partials [splits][H]
+  const int splits2 = db2_splits(h);
+  {
+    LaunchTimer lt(h, s, "w2_transpose_db2", 0.0,
+                   4.0 * F * H + (bias ? 2.0 * T * H + 4.0 * splits2 * H : 0.0));
+    cudaError_t e = launch_transpose_w2(W2, w2t, static_cast<int>(t), H, Fs,
+                                        bias ? dY : nullptr, T, splits2, part2, s);
     lt.done();
     st = from_cuda(e);
   }
@@ -895,11 +905,13 @@ static mlpb_status backward_core(mlpb_handle* h, const void* X, const void* W1, 
                   2.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
 
-  // ---- [s2] db1 = sum_t dZ: the dgrad epilogue's per-warp column sums, added in row order
+  // ---- [s2] db1 = sum_t dZ and db2 = sum_t dY: the dgrad epilogue's per-warp column sums
+  // and the transpose launch's per-range ones, each added in row order, in one launch
   if (st == MLPB_OK && bias) {
     const int np = static_cast<int>(ws_db1_parts(h));
-    LaunchTimer lt(h, s2, "db1_sum", 0.0, 4.0 * np * F + 4.0 * (1 + acc) * F);
-    cudaError_t e = launch_sum_partials(part1, np, F, db1, s2, acc);
+    LaunchTimer lt(h, s2, "bias_sums", 0.0,
+                   4.0 * np * F + 4.0 * splits2 * H + 4.0 * (1 + acc) * (F + H));
+    cudaError_t e = launch_sum_partials_pair(part1, np, F, db1, part2, splits2, H, db2, s2, acc);
     lt.done();
     st = from_cuda(e);
   }
@@ -1001,9 +1013,15 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
                      1.0 * (T * H + F * H) + 4.0 * T * F1 +
                          (bias ? 4.0 * ws_db1_parts(h) * F : 0.0));
   }
-  if (st == MLPB_OK && bias) {  // db2 = sum_t dY on the bf16 dY
-    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * (1 + acc) * H);
-    cudaError_t e = launch_colsum_cluster(dY, T, H, db2, h->num_sms, s, acc);
+  // db2 = sum_t dY on the bf16 dY: the bf16 path's first pass (column sums over row
+  // ranges, without the W2 transpose it shares a launch with there), so that both paths
+  // give the same bits; the ranges are added with db1's partials below
+  float* part2 = reinterpret_cast<float*>(ws + ws_db2_offset(h));
+  const int splits2 = db2_splits(h);
+  if (st == MLPB_OK && bias) {
+    LaunchTimer lt(h, s, "colsum_db2", 0.0, 2.0 * T * H + 4.0 * splits2 * H);
+    cudaError_t e = launch_transpose_w2(nullptr, nullptr, static_cast<int>(t), H, Fs, dY, T,
+                                        splits2, part2, s);
     lt.done();
     st = from_cuda(e);
   }
@@ -1042,10 +1060,11 @@ static mlpb_status backward_f8(mlpb_handle* h, const void* X, const void* W1, co
     st = run_gemm_f8(h, GemmKind::WGRAD_W2, tw2A, tw2B, p, s, "wgrad_w2_f8", 2.0 * H * F * T,
                      1.0 * (T * H + T * F) + 4.0 * (1 + acc) * H * F);
   }
-  if (st == MLPB_OK && bias) {  // db1 = sum_t dZ: the dgrad epilogue's per-warp column sums
+  if (st == MLPB_OK && bias) {  // db1 and db2: the column partial sums, added in row order
     const int np = static_cast<int>(ws_db1_parts(h));
-    LaunchTimer lt(h, s, "db1_sum", 0.0, 4.0 * np * F + 4.0 * (1 + acc) * F);
-    cudaError_t e = launch_sum_partials(part1, np, F, db1, s, acc);
+    LaunchTimer lt(h, s, "bias_sums", 0.0,
+                   4.0 * np * F + 4.0 * splits2 * H + 4.0 * (1 + acc) * (F + H));
+    cudaError_t e = launch_sum_partials_pair(part1, np, F, db1, part2, splits2, H, db2, s, acc);
     lt.done();
     st = from_cuda(e);
   }

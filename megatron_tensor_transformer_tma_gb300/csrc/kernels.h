@@ -35,17 +35,19 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
                                int accumulate = 0);
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s, int accumulate = 0);
-// reduce.cu: the same column sums in one launch (clusters of up to 8 CTAs, one an SM,
-// reduce through distributed shared memory); C % 8 == 0, no scratch.
-cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out, int num_sms,
-                                  cudaStream_t s, int accumulate = 0);
 // Two [nparts][C] partial arrays summed into two outputs in one launch.
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
                                  float* out_a, float* out_b, cudaStream_t s, int accumulate = 0);
+// Two partial arrays of their own sizes ([np_a][C_a], [np_b][C_b]) summed in one launch.
+cudaError_t launch_sum_partials_pair(const float* part_a, int np_a, int64_t C_a, float* out_a,
+                                     const float* part_b, int np_b, int64_t C_b, float* out_b,
+                                     cudaStream_t s, int accumulate = 0);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 // reduce.cu: W2 [t][H][Fs] bf16 -> its per-shard transpose W2t [t][Fs][H] (= [F][H]);
-// H % 64 == 0, Fs % 8 == 0.
+// H % 64 == 0, Fs % 8 == 0.  With dy != NULL the same launch writes the first pass of
+// db2 = sum_t dY [T][H]: part[split][h] over `splits` row ranges (w2 == NULL: only that).
 cudaError_t launch_transpose_w2(const void* w2, void* w2t, int t, int64_t H, int64_t Fs,
+                                const void* dy, int64_t T, int splits, float* part,
                                 cudaStream_t s);
 // reduce.cu: a device copy of `bytes` (a multiple of 16, both pointers 16-byte aligned).
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s);

@@ -119,12 +119,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
 // Whole-cluster barrier (every thread of every CTA in the cluster), release/acquire.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
@@ -136,13 +130,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-
-// 32-bit load from the shared memory of a CTA of the cluster (address from mapa_shared).
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
 }
 
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).

@@ -74,15 +74,6 @@ __global__ void __launch_bounds__(256) colsum_bf16_kernel(const __nv_bfloat16* _
   }
 }
 
-// Single-launch column sums (the backward's db2 = sum_t dY): a cluster of `cs` CTAs (cs <=
-// 8, at most one CTA an SM: the launcher picks the largest cs with chunks x cs <= SMs)
-// owns kCsCols columns and splits the rows into cs contiguous ranges.  In a CTA, warp w
-// reads rows w, w + 8, ... (each warp load is 512 contiguous bytes of one row) and lane l
-// keeps 8 columns; kCsBatch 16-byte loads per thread are issued before any is added.  The
-// 8 row lanes are added in lane order through shared memory, then the cluster's CTA 0
-// adds the CTAs' partial rows in rank order, reading them from their shared memory
-// (distributed shared memory), and writes (or with `accumulate` adds to) out.  No second
-// launch, no atomics: reproducible bit for bit.
 // A 16-byte streaming load (read once: no L1 allocation).  An asm volatile, so that a
 // batch of them is issued in program order before the adds that consume it.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -93,71 +84,22 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
-constexpr int kCsMaxCluster = 8;
-constexpr int kCsCols = 256;
-constexpr int kCsRowLanes = 8;
-constexpr int kCsBatch = 24;
-
-__global__ void __launch_bounds__(256, 1)
-    colsum_cluster_kernel(const __nv_bfloat16* __restrict__ in, int64_t R, int64_t C,
-                          float* __restrict__ out, int accumulate) {
-  __shared__ float red[kCsRowLanes][kCsCols];
-  const int lane = threadIdx.x & 31, rl = threadIdx.x >> 5;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t cs = cluster_nctarank();
-  const int64_t chunk = blockIdx.x / cs;
-  const int64_t col = chunk * kCsCols + lane * 8;
-  const int64_t rpc = (R + cs - 1) / cs;
-  const int64_t r0 = rank * rpc;
-  const int64_t r1 = min(R, r0 + rpc);
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  if (col < C) {
-    const int64_t step = kCsRowLanes * C;  // elements between a lane's consecutive rows
-    int64_t r = r0 + rl;
-    const __nv_bfloat16* p = in + r * C + col;
-    for (; r + (kCsBatch - 1) * kCsRowLanes < r1; r += kCsBatch * kCsRowLanes) {
-      uint4 u[kCsBatch];
-#pragma unroll
-      for (int j = 0; j < kCsBatch; ++j) u[j] = ld_stream_v4(p + j * step);
-#pragma unroll
-      for (int j = 0; j < kCsBatch; ++j) add_bf16x8(u[j], acc);
-      p += kCsBatch * step;
-    }
-    for (; r < r1; r += kCsRowLanes, p += step) add_bf16x8(ld_global_nc_v4(p), acc);
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) red[rl][lane * 8 + e] = acc[e];
-  __syncthreads();
-  const int c = threadIdx.x;  // one column a thread from here on
-  float s = 0.f;
-#pragma unroll
-  for (int l = 0; l < kCsRowLanes; ++l) s += red[l][c];
-  __syncthreads();
-  red[0][c] = s;
-  cluster_sync();  // every CTA's partial row is written
-  if (rank == 0 && chunk * kCsCols + c < C) {
-    const uint32_t a = smem_u32(&red[0][c]);
-    float t = 0.f;
-    for (uint32_t q = 0; q < cs; ++q) t += ld_shared_cluster_f32(mapa_shared(a, q));
-    float* o = out + chunk * kCsCols + c;
-    *o = accumulate ? *o + t : t;
-  }
-  cluster_sync();  // the peers' shared memory stays until CTA 0 has read it
-}
-
 // out[c] = sum_k part[k][c] (or out[c] += ... with `accumulate`) for one or two partial
-// arrays (blockIdx.y picks the array).
+// arrays (blockIdx.y picks the array; each has its own part count and width).
 // A CTA owns 32 columns: warp w sums parts w, w+8, ... of its lane's column, then the
 // eight warp sums are added in warp order -- a fixed order, so results are reproducible.
-__global__ void __launch_bounds__(256) sum_partials_kernel(const float* part_a,
-                                                           const float* part_b, int nparts,
-                                                           int64_t C, float* out_a,
-                                                           float* out_b, int accumulate) {
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float* part_a, int np_a,
+                                                           int64_t C_a, float* out_a,
+                                                           const float* part_b, int np_b,
+                                                           int64_t C_b, float* out_b,
+                                                           int accumulate) {
   __shared__ float red[8][33];
-  const float* part = blockIdx.y == 0 ? part_a : part_b;
-  float* out = blockIdx.y == 0 ? out_a : out_b;
+  const bool second = blockIdx.y != 0;
+  const float* part = second ? part_b : part_a;
+  float* out = second ? out_b : out_a;
+  const int nparts = second ? np_b : np_a;
+  const int64_t C = second ? C_b : C_a;
+  if (static_cast<int64_t>(blockIdx.x) * 32 >= C) return;  // the narrower array's spare CTAs
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float s = 0.f;
@@ -194,37 +136,27 @@ cudaError_t launch_colsum_bf16(const void* in, int64_t R, int64_t C, int splits,
   return launch_sum_partials(part, splits, C, out, s, accumulate);
 }
 
-cudaError_t launch_colsum_cluster(const void* in, int64_t R, int64_t C, float* out, int num_sms,
-                                  cudaStream_t s, int accumulate) {
-  const int64_t chunks = (C + kCsCols - 1) / kCsCols;
-  const int cs = static_cast<int>(std::max<int64_t>(
-      1, std::min<int64_t>(kCsMaxCluster, num_sms / std::max<int64_t>(1, chunks))));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(chunks * cs), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, colsum_cluster_kernel, static_cast<const __nv_bfloat16*>(in),
-                            R, C, out, accumulate);
-}
-
 cudaError_t launch_sum_partials(const float* part, int nparts, int64_t C, float* out,
                                 cudaStream_t s, int accumulate) {
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 1);
-  sum_partials_kernel<<<grid, 256, 0, s>>>(part, part, nparts, C, out, out, accumulate);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part, nparts, C, out, part, nparts, C, out,
+                                           accumulate);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int nparts, int64_t C,
                                  float* out_a, float* out_b, cudaStream_t s, int accumulate) {
+  return launch_sum_partials_pair(part_a, nparts, C, out_a, part_b, nparts, C, out_b, s,
+                                  accumulate);
+}
+
+cudaError_t launch_sum_partials_pair(const float* part_a, int np_a, int64_t C_a, float* out_a,
+                                     const float* part_b, int np_b, int64_t C_b, float* out_b,
+                                     cudaStream_t s, int accumulate) {
+  const int64_t C = C_a > C_b ? C_a : C_b;
   const dim3 grid(static_cast<unsigned>((C + 31) / 32), 2);
-  sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, part_b, nparts, C, out_a, out_b, accumulate);
+  sum_partials_kernel<<<grid, 256, 0, s>>>(part_a, np_a, C_a, out_a, part_b, np_b, C_b, out_b,
+                                           accumulate);
   return cudaGetLastError();
 }
 
@@ -234,14 +166,12 @@ cudaError_t launch_sum_partials2(const float* part_a, const float* part_b, int n
 // moves a 64 (h) x 128 (j) tile: eight lanes load each 128-byte run of a W2 row, and eight
 // lanes store each 128-byte run of a W2t row, so both sides move whole lines.
 // H % 64 == 0, Fs % 8 == 0.
-__global__ void __launch_bounds__(256) transpose_w2_kernel(const __nv_bfloat16* __restrict__ w2,
-                                                          __nv_bfloat16* __restrict__ w2t,
-                                                          int H, int Fs) {
-  // Shared memory holds the tile transposed as 32-bit words, each the pair (h, h + 1) at
-  // one f: row f of 32 words (+1 of padding) is the 128-byte run of row f of the copy.
-  __shared__ uint32_t tileT[128][33];
-  const int i = blockIdx.z;
-  const int h0 = blockIdx.y * 64, f0 = blockIdx.x * 128;
+__device__ __forceinline__ void transpose_w2_tile(const __nv_bfloat16* __restrict__ w2,
+                                                  __nv_bfloat16* __restrict__ w2t, int H, int Fs,
+                                                  int fx, int hy, int i, uint32_t (*tileT)[33]) {
+  // tileT holds the tile transposed as 32-bit words, each the pair (h, h + 1) at one f:
+  // row f of 32 words (+1 of padding) is the 128-byte run of row f of the copy.
+  const int h0 = hy * 64, f0 = fx * 128;
   const int c8 = threadIdx.x & 7, p = threadIdx.x >> 3;  // f chunk of 8, h pair
   const __nv_bfloat16* src = w2 + (static_cast<size_t>(i) * H + h0 + 2 * p) * Fs + f0;
   uint4 u[2][2];
@@ -277,13 +207,82 @@ __global__ void __launch_bounds__(256) transpose_w2_kernel(const __nv_bfloat16* 
   }
 }
 
+constexpr int kTcBatch = 4;  // 16-byte loads in flight a thread in the column-sum blocks
+
+// The start of the bf16 backward in one launch.  Blocks [0, n_tr) write W2's transposed
+// copy, one 64 x 128 tile each (tiles in (f, h, shard) order).  With a bias, blocks
+// [n_tr, n_tr + chunks * splits) take the first pass of db2 = sum_t dY: block (split,
+// chunk) sums the 256 columns of `chunk` over its row range; warp w reads rows w, w + 8,
+// ... (each warp load is 512 contiguous bytes of one row), kTcBatch loads in flight a
+// thread, and the 8 warps' partial rows are added in warp order through shared memory
+// into part[split][256 chunk ..] (a fixed order: reproducible).  Both halves are DRAM
+// streams; the column sums fill the GPU beside the transpose instead of in a launch of
+// their own, and the final sum over the splits joins db1's.  At most 40 registers a
+// thread (6 CTAs an SM), for the transpose's loads in flight.
+__global__ void __launch_bounds__(256, 6)
+    transpose_w2_colsum_kernel(const __nv_bfloat16* __restrict__ w2,
+                               __nv_bfloat16* __restrict__ w2t, int H, int Fs, int n_tr,
+                               const __nv_bfloat16* __restrict__ dy, int64_t T, int64_t rps,
+                               float* __restrict__ part) {
+  __shared__ __align__(16) uint32_t smem[128 * 33];
+  const int b = blockIdx.x;
+  if (b < n_tr) {
+    const int ntx = (Fs + 127) / 128, nty = H / 64;
+    const int i = b / (ntx * nty);
+    const int r = b - i * ntx * nty;
+    const int hy = r / ntx;
+    transpose_w2_tile(w2, w2t, H, Fs, r - hy * ntx, hy, i,
+                      reinterpret_cast<uint32_t (*)[33]>(smem));
+    return;
+  }
+  const int chunks = (H + 255) / 256;
+  const int cb = b - n_tr;
+  const int split = cb / chunks, chunk = cb - split * chunks;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t col = static_cast<int64_t>(chunk) * 256 + lane * 8;
+  const int64_t r0 = static_cast<int64_t>(split) * rps;
+  const int64_t r1 = min(T, r0 + rps);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (col < H) {
+    const int64_t step = 8 * static_cast<int64_t>(H);
+    int64_t r = r0 + w;
+    const __nv_bfloat16* p = dy + r * H + col;
+    for (; r + (kTcBatch - 1) * 8 < r1; r += kTcBatch * 8) {
+      uint4 u[kTcBatch];
+#pragma unroll
+      for (int j = 0; j < kTcBatch; ++j) u[j] = ld_stream_v4(p + j * step);
+#pragma unroll
+      for (int j = 0; j < kTcBatch; ++j) add_bf16x8(u[j], acc);
+      p += kTcBatch * step;
+    }
+    for (; r < r1; r += 8, p += step) add_bf16x8(ld_global_nc_v4(p), acc);
+  }
+  float (*red)[256] = reinterpret_cast<float (*)[256]>(smem);  // [8][256]
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc[e];
+  __syncthreads();
+  const int c = threadIdx.x;
+  if (static_cast<int64_t>(chunk) * 256 + c < H) {
+    float t = 0.f;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) t += red[l][c];
+    part[static_cast<int64_t>(split) * H + static_cast<int64_t>(chunk) * 256 + c] = t;
+  }
+}
+
 cudaError_t launch_transpose_w2(const void* w2, void* w2t, int t, int64_t H, int64_t Fs,
+                                const void* dy, int64_t T, int splits, float* part,
                                 cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((Fs + 127) / 128), static_cast<unsigned>(H / 64),
-                  static_cast<unsigned>(t));
-  transpose_w2_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w2),
-                                           static_cast<__nv_bfloat16*>(w2t), static_cast<int>(H),
-                                           static_cast<int>(Fs));
+  const int64_t n_tr = w2 != nullptr ? ((Fs + 127) / 128) * (H / 64) * t : 0;
+  const int64_t n_cs = dy != nullptr ? ((H + 255) / 256) * splits : 0;
+  const int64_t rps = splits > 0 ? (T + splits - 1) / splits : 0;
+  if (n_tr + n_cs == 0) return cudaSuccess;
+  transpose_w2_colsum_kernel<<<static_cast<unsigned>(n_tr + n_cs), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(w2), static_cast<__nv_bfloat16*>(w2t),
+      static_cast<int>(H), static_cast<int>(Fs), static_cast<int>(n_tr),
+      static_cast<const __nv_bfloat16*>(dy), T, rps, part);
   return cudaGetLastError();
 }
 

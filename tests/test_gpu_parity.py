@@ -70,13 +70,12 @@ def test_timing_records_and_serialised_schedule_are_bitwise_equal():
     for k in ("Y", "dX", "dW1", "dW2", "db1", "db2", "Z", "A"):
         assert torch.equal(a[k], b[k]), k
     recs = b["timings"]
-    assert [r["name"] for r in recs] == ["fc1_gelu", "fc2", "colsum_db2", "w2_transpose",
-                                         "dgrad_gelu", "wgrad_w2", "db1_sum", "wgrad_w1",
-                                         "dgrad_x"]
+    assert [r["name"] for r in recs] == ["fc1_gelu", "fc2", "w2_transpose_db2", "dgrad_gelu",
+                                         "wgrad_w2", "bias_sums", "wgrad_w1", "dgrad_x"]
     T, H, F = shape.tokens, shape.hidden, shape.ffn
     for r in recs:
         assert r["ms"] > 0.0 and r["bytes"] > 0.0 and r["kernels"] == 1
-        if r["name"] in ("colsum_db2", "db1_sum", "w2_transpose"):
+        if r["name"] in ("w2_transpose_db2", "bias_sums"):
             assert r["flops"] == 0.0
         else:
             assert r["flops"] == 2.0 * T * H * F
