@@ -102,29 +102,81 @@ __device__ __forceinline__ void unit_range(int u, int split, int split_start, in
 // tanh-form GELU written with s = sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3): since
 // 1 + tanh(u) = 2 sigmoid(2u), gelu(z) = z s, the same function without cancellation for
 // z << 0, and gelu'(z) = s + z s (1 - s) 2 sqrt(2/pi) (1 + 3 * 0.044715 z^2).  The
-// constants are folded so that e^{-2u} is one exponential of z (a + b z^2):
-//   e^{-2u} = exp(z (-2k - 2k c z^2)),  k = sqrt(2/pi), c = 0.044715.
+// constants are folded so that e^{-2u} = 2^{z (a + b z^2)} is one base-2 exponential:
+//   a = -2k log2(e), b = -2k c log2(e),  k = sqrt(2/pi), c = 0.044715.
 // For |z| past ~10 the exponential overflows to +inf (s = 0) or underflows to 0 (s = 1),
 // and both forms then return their limits (0 and z; 0 and 1) with no inf * 0.
 constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kGeluCubic = 0.044715f;
-constexpr float kGeluA = -2.0f * kSqrt2OverPi;                 // -2k
-constexpr float kGeluB = -2.0f * kSqrt2OverPi * kGeluCubic;    // -2kc
-constexpr float kGeluD0 = 2.0f * kSqrt2OverPi;                 // 2k
-constexpr float kGeluD2 = 6.0f * kSqrt2OverPi * kGeluCubic;    // 6kc
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kGeluA = -2.0f * kSqrt2OverPi * kLog2e;               // -2k log2(e)
+constexpr float kGeluB = -2.0f * kSqrt2OverPi * kGeluCubic * kLog2e;  // -2kc log2(e)
+constexpr float kGeluD0 = 2.0f * kSqrt2OverPi;                        // 2k
+constexpr float kGeluD2 = 6.0f * kSqrt2OverPi * kGeluCubic;           // 6kc
 
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
-__device__ __forceinline__ float gelu_f(float z) {
-  const float t = __expf(z * fmaf(kGeluB, z * z, kGeluA));  // e^{-2u}
-  return z * __fdividef(1.0f, 1.0f + t);
+// 2^x (the MUFU base-2 exponential; subnormal results flush to zero).
+__device__ __forceinline__ float ex2_f(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
-__device__ __forceinline__ float gelu_grad_f(float z) {
-  const float z2 = z * z;
-  const float s = __fdividef(1.0f, 1.0f + __expf(z * fmaf(kGeluB, z2, kGeluA)));
-  const float d = z * fmaf(kGeluD2, z2, kGeluD0);  // 2k z (1 + 3c z^2)
-  return fmaf(d, fmaf(-s, s, s), s);               // s + d s (1 - s)
+// Two fp32 values in one 64-bit register (lo in the low half) and the f32x2 arithmetic
+// of the sm_100 family: one instruction for both lanes, each rounded as its fp32 form.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// e^{-2u} + 1 for two values of z (one MUFU exponential each), and its reciprocal s.
+__device__ __forceinline__ uint64_t gelu_s_x2(uint64_t z, uint64_t z2) {
+  float u0, u1, d0, d1;
+  f2_unpack(f2_mul(z, f2_fma(z2, f2_pack(kGeluB, kGeluB), f2_pack(kGeluA, kGeluA))), u0, u1);
+  f2_unpack(f2_add(f2_pack(ex2_f(u0), ex2_f(u1)), f2_pack(1.0f, 1.0f)), d0, d1);
+  return f2_pack(__fdividef(1.0f, d0), __fdividef(1.0f, d1));
+}
+
+// gelu(z) = z s for two values.
+__device__ __forceinline__ uint64_t gelu_x2(uint64_t z) { return f2_mul(z, gelu_s_x2(z, f2_mul(z, z))); }
+
+// gelu'(z) = s + d s (1 - s), d = 2k z (1 + 3c z^2), for two values.
+__device__ __forceinline__ uint64_t gelu_grad_x2(uint64_t z) {
+  const uint64_t z2 = f2_mul(z, z);
+  const uint64_t s = gelu_s_x2(z, z2);
+  const uint64_t d = f2_mul(z, f2_fma(z2, f2_pack(kGeluD2, kGeluD2), f2_pack(kGeluD0, kGeluD0)));
+  return f2_fma(d, f2_sub(s, f2_mul(s, s)), s);
+}
+
+// v[e] = gelu(v[e]) over 32 values, two at a time.
+__device__ __forceinline__ void gelu_x32(float (&v)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) f2_unpack(gelu_x2(f2_pack(v[e], v[e + 1])), v[e], v[e + 1]);
 }
 
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid, float (&v)[32]) {
@@ -262,11 +314,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
         float b[32];
         load_bf16x32(p.bias + col, nv, b);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] += b[e];
+        for (int e = 0; e < 32; e += 2)
+          f2_unpack(f2_add(f2_pack(v[e], v[e + 1]), f2_pack(b[e], b[e + 1])), v[e], v[e + 1]);
       }
       if (row_ok) store_bf16x32(Z + col, nv, v);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
+      gelu_x32(v);
       if (row_ok) {
         store_bf16x32(A + col, nv, v);
         if constexpr (F8) track_amax(v, nv, am);
@@ -356,11 +408,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
           if (A != nullptr) {
             float a[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = gelu_f(z[e]);
+            for (int e = 0; e < 32; ++e) a[e] = z[e];
+            gelu_x32(a);
             store_bf16x32(A + f, nv, a);
           }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= gelu_grad_f(z[e]);
+          for (int e = 0; e < 32; e += 2)
+            f2_unpack(f2_mul(f2_pack(v[e], v[e + 1]), gelu_grad_x2(f2_pack(z[e], z[e + 1]))),
+                      v[e], v[e + 1]);
           pack_bf16x32(v, w);
           store_packed_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, nv, w);
           if constexpr (F8) track_amax(v, nv, am);
