@@ -577,7 +577,8 @@ __device__ __forceinline__ void step_kpos(KPos& kp, bool rev, const GemmParams& 
 }
 
 // One stage of one CTA of the pair: its own 128 A rows, and its 128-row half of B (K-major:
-// one box; MN-major: two 64-wide chunks).
+// one box; MN-major: two 64-wide chunks, in one copy through a 3-D map when GemmParams.mn3d
+// says so, else two).
 // FP8: every operand is K-major (E4M3 copies, transposed where needed), one box each:
 //   FC1  A Xq [T][H]            B W1q [F][H] / [t][2][Fs][H]
 //   FC2  A Aq [T][t][Fs]        B W2q [t][H][Fs]             (K walks the shards)
