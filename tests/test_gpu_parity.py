@@ -31,6 +31,9 @@ SMALL = [
     pytest.param(MLPShape(128, 128, 512, 2, "gelu", True, sp_ln=True), 17, id="sp-ln-gelu-t2"),
     # 80 pair tiles on 76 pairs: fc2 and dX split their 4 tail tiles' K range 4 ways
     pytest.param(MLPShape(1024, 5120, 2048, 2, "gelu", True), 18, id="gelu-tail-split"),
+    # T = 640: five 128-row M tiles (the last pair's odd CTA has no rows), and db2's column
+    # sums over two row ranges of 320; F = 1344 (21 chunks of 64: the MN-major 3-D maps)
+    pytest.param(MLPShape(640, 320, 1344, 4, "gelu", True), 20, id="gelu-t4-T640-oddM"),
 ]
 
 
