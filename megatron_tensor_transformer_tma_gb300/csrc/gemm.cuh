@@ -495,14 +495,17 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, int row, int mt, in
       if (row_ok) {
         const int nv = min(32, p.H - col);
         float* q = dW + static_cast<size_t>(col) * p.Fs;
+        if (p.accumulate) {  // all 32 reads in flight before the first write
+          float old[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < nv) {
-            float r = v[e];
-            if (p.accumulate) r += __ldcg(q + static_cast<size_t>(e) * p.Fs);
-            q[static_cast<size_t>(e) * p.Fs] = r;
-          }
+          for (int e = 0; e < 32; ++e)
+            old[e] = e < nv ? __ldcg(q + static_cast<size_t>(e) * p.Fs) : 0.0f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] += old[e];
         }
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e < nv) q[static_cast<size_t>(e) * p.Fs] = v[e];
       }
     }
   } else {  // WGRAD_W1
